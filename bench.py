@@ -1,0 +1,387 @@
+"""Benchmark of the GB300 two-level candidate indexer.
+
+One step = one pass of the whole indexer path over one batch of synthetic
+input: the source layer's dense block keys, its published candidate blocks,
+its own top-512 and the four consumer layers' top-512.  The headline workload
+is the 16384-row prefill chunk at 262144 compressed positions; the decode
+batches are reported as secondary lines in the same JSON object.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
+indexer has no exchange step, so no collective touches the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+HEADLINE_CID = 4
+METRIC = "indexer ms per 16K-token prefill chunk @262K ctx"
+PAGES_LAST_CHUNK_MS = 78.2  # sglang PR #40352 Performance table: PR's indexer kernels, last chunk (4x B200)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_counts(wl):
+    """FLOPs of the dense pass and bytes of index-K it must read.
+
+    Dense scorer: 2 * H * D flops per (row, position) over rows with more than
+    K blocks.  Bytes: 132 per position of K (128 e4m3 + 4-byte scale) read
+    once per launch -- the pool of a prefill chunk, every scored row's own
+    positions in decode -- plus the query and weights of scored rows.
+    """
+    L = wl.seq_len.to(torch.int64).cpu()
+    nb = (L + 7) // 8
+    scored = nb > wl.topk_blocks
+    positions = int(L[scored].sum())
+    flops = 2 * 64 * 128 * positions
+    if wl.layout == 1:
+        kbytes = 132 * (int(L.max()) if bool(scored.any()) else 0)
+    else:
+        kbytes = 132 * positions
+    qbytes = int(scored.sum()) * (64 * 64 + 64 * 4 + 64 * 4)
+    return flops, kbytes + qbytes, positions
+
+
+def time_steps(step, steps, warmup, flush, stream, dense_events=True):
+    """Per-step and per-dense-kernel CUDA-event durations (ms) on `stream`."""
+    from two_level_sparse_gb300 import ci
+
+    wl = step.wl
+    for _ in range(warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    t_step, t_dense = [], []
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()  # evict L2 between steps (same stream, before the first event: not timed)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        src = wl.layers[0]
+        ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, wl.page_table, wl.layout, wl.seq_len,
+                                step.max_len, step.K, step.keys, dev_err=step.dev_err, stream=stream)
+        ev[1].record(stream)
+        step.run_after_dense(stream)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        t_dense.append(ev[0].elapsed_time(ev[1]))
+        t_step.append(ev[0].elapsed_time(ev[2]))
+    return t_step, t_dense
+
+
+def e2e_time(step, host_inputs, steps, stream):
+    """The same step through the C ABI with host buffers: pinned host -> device
+    copies of the step's inputs, the step, and device -> host of its results,
+    all inside the timed region."""
+    wl = step.wl
+    dev_tensors = [wl.seq_len, wl.page_table] + [t for l in wl.layers for t in (l.q_fp4, l.q_sf, l.w, l.k_pool)]
+    outs = [step.pos, step.blocks, step.nvalid]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    times = []
+    for _ in range(steps + 1):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for d, h in zip(dev_tensors, host_inputs):
+                d.copy_(h, non_blocking=True)
+            step.run(stream)
+            for h, o in zip(host_out, outs):
+                h.copy_(o, non_blocking=True)
+        stream.synchronize()
+        times.append((time.perf_counter() - t0) * 1e3)
+    return times[1:], h2d, d2h
+
+
+def cpu_oracle_sample(cid, budget_s=20.0):
+    """The oracle as it stands, on the host cores, over a bounded row sample of
+    workload `cid`; returns (ms per step extrapolated, rows timed, threads)."""
+    import numpy as np
+
+    from oracle import ci_oracle as O
+    from two_level_sparse_gb300 import synth
+
+    lens = synth.config_lengths(cid)
+    rows = [int(lens.shape[0]) - 1, 0, int(lens.shape[0]) // 2]
+    # operands of the sampled rows only (the whole pool comes along)
+    wl = synth.config_workload(cid, device="cuda" if torch.cuda.is_available() else "cpu")
+    pt = wl.page_table.cpu().numpy()
+    layers = [synth.Layer(l.q_fp4[rows].cpu(), l.q_sf[rows].cpu(), l.w[rows].cpu(), l.k_pool.cpu()) for l in wl.layers]
+    pts = pt[rows] if wl.layout == 0 else pt
+    K, P = wl.topk_blocks, wl.topk
+    done, t_total = 0, 0.0
+    for i, t in enumerate(rows):
+        L = int(lens[t])
+        t0 = time.perf_counter()
+        src = O.source_row(layers[0], pts, wl.layout, i, L, max(K, P + 1), P)
+        blocks, nv = O.select_blocks(src["keys"], O.num_blocks(L), K)
+        for j in range(1, len(layers)):
+            O.select_row(layers[j], pts, wl.layout, i, L, blocks, nv, P)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total > budget_s:
+            break
+    del wl
+    torch.cuda.empty_cache() if torch.cuda.is_available() else None
+    per_row = t_total / done
+    threads = torch.get_num_threads()
+    try:
+        import threadpoolctl
+
+        info = threadpoolctl.threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    return per_row * int(lens.shape[0]) * 1e3, done, threads, int(lens.shape[0])
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    ms_per_step, done, threads, nrows = cpu_oracle_sample(HEADLINE_CID, budget_s=15.0)
+    steps = []
+    for _ in range(args.warmup + args.steps):
+        m, done, threads, nrows = cpu_oracle_sample(HEADLINE_CID, budget_s=5.0)
+        steps.append(m)
+    value = statistics.mean(steps[args.warmup:]) if args.steps else ms_per_step
+    sample = f"{done} of {nrows} rows per step, timed and extrapolated linearly to the chunk"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill_16384rows_ctx262144_K2048", "rows": 16384, "context": 262144,
+                   "topk_blocks": 2048, "topk": 512, "layers": 5},
+        "cpu_baseline": {"value": value, "unit": "ms", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+class BenchStep:
+    """IndexerStep whose dense launch can be timed separately."""
+
+    def __init__(self, wl):
+        from two_level_sparse_gb300.step import IndexerStep
+
+        self.inner = IndexerStep(wl)
+        self.wl = wl
+
+    def __getattr__(self, k):
+        return getattr(self.inner, k)
+
+    def run(self, stream=None):
+        self.inner.run(stream)
+
+    def run_after_dense(self, stream=None):
+        self.inner.run(stream, skip_dense=True)
+
+
+def measure(cid, steps, warmup, stream, flush, e2e=False):
+    from two_level_sparse_gb300 import synth
+
+    wl = synth.config_workload(cid, device="cuda")
+    step = BenchStep(wl)
+    t_step, t_dense = time_steps(step, steps, warmup, flush, stream)
+    res = {"cid": cid, "wl": wl, "step": step, "t_step": t_step, "t_dense": t_dense,
+           "launches": step.inner.launches()}
+    if e2e:
+        host = [t.cpu().pin_memory() for t in [wl.seq_len, wl.page_table] +
+                [x for l in wl.layers for x in (l.q_fp4, l.q_sf, l.w, l.k_pool)]]
+        res["e2e"] = e2e_time(step.inner, host, max(2, min(steps, 5)), stream)
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from two_level_sparse_gb300 import ci  # noqa: F401  (fails loudly without the library)
+
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    peaks, peak_src = load_peaks()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        head = measure(HEADLINE_CID, args.steps, args.warmup, stream, flush, e2e=True)
+        barrier()
+        wall = time.perf_counter() - t0
+    ms_step = statistics.mean(head["t_step"])
+    ms_dense = statistics.mean(head["t_dense"])
+    if world > 1:
+        t = torch.tensor([ms_step, ms_dense], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, ms_dense = t.tolist()
+    wl = head["wl"]
+    err = int(head["step"].dev_err.item())
+    flops, kbytes, positions = algorithmic_counts(wl)
+    fp8_peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    achieved = flops / (ms_dense * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = head["e2e"]
+    e2e_val = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_val], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_val = t.item()
+
+    secondary = []
+    if not args.no_secondary:
+        del head
+        torch.cuda.empty_cache()
+        for cid in (2, 1):
+            r = measure(cid, max(3, args.steps // 2), 3, stream, flush)
+            mst = statistics.mean(r["t_step"])
+            msd = statistics.mean(r["t_dense"])
+            f, b, _ = algorithmic_counts(r["wl"])
+            rows = r["wl"].rows
+            secondary.append({
+                "metric": "decode rows/s", "workload": r["wl"].name, "value": world * rows / (mst * 1e-3),
+                "unit": "rows/s", "ms_per_step": mst, "dense_ms": msd,
+                "dense_roofline": {"bound": "hbm", "achieved": b / (msd * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": b / (msd * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                "dev_err": int(r["step"].dev_err.item()),
+            })
+            del r
+            torch.cuda.empty_cache()
+
+    cpu_ms, cpu_rows, cpu_threads, nrows = (None, 0, 0, 0)
+    if rank == 0:
+        cpu_ms, cpu_rows, cpu_threads, nrows = cpu_oracle_sample(HEADLINE_CID, budget_s=15.0)
+    value = ms_step / world
+    line = {
+        "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": value / PAGES_LAST_CHUNK_MS, "dtype": "e4m3xe4m3->f32 (mxf8f6f4, ue8m0 scales)",
+        "data": "synthetic",
+        "config": {"workload": "prefill_16384rows_ctx262144_K2048", "rows": 16384, "context": 262144,
+                   "topk_blocks": 2048, "topk": 512, "layers": 5, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (256 MiB write)"},
+        "roofline": {"bound": "tensor", "kernel": "dense_amax8_kernel", "achieved": achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained x2 (fp8 / bf16 nominal ratio)",
+                     "flops_per_launch": flops, "dense_ms": ms_dense},
+        "e2e": {"value": e2e_val / world, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": head_launches(args.steps, world),
+        "clocks": clk.summary(),
+        "wall_s": wall,
+        "dev_err": err,
+        "secondary": secondary,
+        "cpu_baseline": None if cpu_ms is None else {
+            "value": cpu_ms, "unit": "ms", "cores": cpu_threads, "kind": "oracle",
+            "sample": f"{cpu_rows} of {nrows} rows (last, first, middle), all 5 layers, extrapolated linearly"},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def head_launches(steps, world):
+    # per step: dense 1 + publish 1 + select 5 (K' == K at the headline workload)
+    return steps * 7
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+/*
+ * ci.h -- C ABI of the GB300 two-level candidate indexer (libci.so).
+ *
+ * The DeepSeek-V4.1 indexer picks, for every query row t, the compressed
+ * positions s < L_t that sparse attention will read.  It works in two levels
+ * (sglang PR #40352 "Score prefill consumer index layers on candidate blocks
+ * with DeepGEMM", Motivation and Design; sglang PR #39671 "dsv4.1: candidate
+ * indexer library", Summary):
+ *
+ *   level one, once per step, on the source index layer:
+ *     ci_score_dense_amax8   logit[t,s] = sum_h w[t,h] * ReLU(q[t,h] . k[s])
+ *                            for every s < L_t, reduced on chip to one key per
+ *                            block of 8 positions (the block maximum), the
+ *                            row's newest block forced to +inf;
+ *     ci_publish_blocks      each row's top topk_blocks block ids by key,
+ *                            ascending, INT32_MAX padded;
+ *   level two, once per layer (the source itself and each consumer):
+ *     ci_select_sparse       scores only the positions inside a row's
+ *                            published blocks and returns its top-k positions,
+ *                            ascending, -1 padded.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - H = 64 heads, D = 128 dims, blocks of 8 positions, pages of 64 positions.
+ *  - All array arguments are DEVICE pointers owned by the caller.  The library
+ *    allocates nothing, never synchronizes the device or the stream, records
+ *    no events, and enqueues its kernels on `stream` (a cudaStream_t; NULL =
+ *    the legacy default stream).
+ *  - Query (MXFP4): q_fp4 uint8 [rows][64][64], two e2m1 codes per byte,
+ *    element 2i in the low nibble; q_sf uint8 [rows][64][4], one ue8m0 scale
+ *    per 32 elements (vLLM sparse_attn_indexer.py, "MXFP4 layout" comment).
+ *  - Head weights: w float [rows][64].
+ *  - Index-K pool: k_pool uint8 [num_pages][8448].  Page p holds 64 positions:
+ *    bytes [0, 8192) are their FP8 e4m3 vectors (128 bytes each), bytes
+ *    [8192, 8448) their fp32 scales (little endian).  The scale multiplies the
+ *    decoded vector.  k_pool must be 16-byte aligned.
+ *  - Page table: page_table int32 [num_req][max_pages]; logical page j of a
+ *    request lives in physical page page_table[req][j].  Position s of a row
+ *    is slot s % 64 of logical page s / 64.
+ *  - Row layout (`layout`):
+ *      CI_LAYOUT_DECODE  row t is request t (num_req == rows);
+ *      CI_LAYOUT_PREFILL all rows belong to request 0 (num_req == 1) and share
+ *                        its pages; row t reaches its first L_t positions.
+ *  - seq_len int32 [rows]: L_t, with 0 <= L_t <= max_len <= 64 * max_pages.
+ *    max_len is the caller's host-side bound; the kernels check every L_t
+ *    against it on the device.
+ *  - dev_err: optional (may be NULL) device int32.  Kernels OR CI_DEVERR_*
+ *    bits into it when they meet data that breaks the contract (a length above
+ *    max_len, a page id outside [0, num_pages), a block id out of range); the
+ *    offending row or tile is skipped and its outputs are undefined.  The
+ *    caller clears it and reads it back when convenient.
+ *  - Return value: CI_OK or a negative CI_ERR_* code from the host-side
+ *    argument checks (nothing is launched then), or CI_ERR_CUDA if a launch
+ *    failed.  ci_strerror() names the code.
+ *  - Ties are broken toward the lower index, for blocks and for positions.
+ */
+#ifndef CI_H_
+#define CI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CI_API __attribute__((visibility("default")))
+#else
+#define CI_API
+#endif
+
+#define CI_HEADS 64
+#define CI_DIM 128
+#define CI_BLOCK 8
+#define CI_PAGE 64
+#define CI_PAGE_BYTES (CI_PAGE * CI_DIM + CI_PAGE * 4)
+
+enum ci_status {
+  CI_OK = 0,
+  CI_ERR_NULL = -1,        /* a required pointer is NULL */
+  CI_ERR_SHAPE = -2,       /* inconsistent sizes or strides */
+  CI_ERR_ALIGN = -3,       /* a pointer or stride breaks an alignment rule */
+  CI_ERR_RANGE = -4,       /* a size is out of its supported range */
+  CI_ERR_UNSUPPORTED = -5, /* a valid request this build does not implement */
+  CI_ERR_CUDA = -6         /* a CUDA call failed (launch or attribute) */
+};
+
+enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1 };
+
+/* Bits OR-ed into *dev_err by the kernels. */
+#define CI_DEVERR_LEN 1u     /* seq_len[t] < 0 or > max_len */
+#define CI_DEVERR_PAGE 2u    /* page id outside [0, num_pages) */
+#define CI_DEVERR_BLOCK 4u   /* candidate block id outside [0, ceil(L_t/8)) or nvalid out of range */
+#define CI_DEVERR_TIMEOUT 8u /* an on-chip pipeline wait gave up (should never happen) */
+
+/*
+ * Level one, scoring: block keys of the source layer.
+ *
+ * For every row t with nb_t = ceil(L_t / 8) > skip_le_blocks and every block
+ * b < nb_t writes
+ *     keys[t * keys_stride + b] = max_{8b <= s < min(8b + 8, L_t)} logit[t, s]
+ * with logit[t, s] = kscale[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s]) computed in
+ * fp32 (products exact, fp32 accumulation), and keys[t*keys_stride + nb_t - 1]
+ * = +inf.  Rows with nb_t <= skip_le_blocks are not scored and their keys are
+ * left untouched (sglang PR #40352, Design, "Level one"; the block_amax.cuh
+ * listing in the same PR's review: max of 8, last key +inf, rows with at most
+ * topk blocks skipped).  The [rows, L] score matrix is never written.
+ *
+ * keys: float [rows][keys_stride], 16-byte aligned, keys_stride % 8 == 0 and
+ * keys_stride >= ceil(max_len / 8).
+ */
+CI_API int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
+                         int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                         int32_t layout, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                         int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
+                         void* stream);
+
+/*
+ * Level one, publishing: each row's candidate blocks.
+ *
+ * For every row t: if nb_t <= topk_blocks, blocks[t][0..nb_t) = 0..nb_t-1
+ * (keep everything, keys not read); otherwise the topk_blocks block ids with
+ * the largest keys (ties: lower id first).  The ids are written ascending into
+ * blocks[t * blocks_stride + i], i < topk_blocks, the rest of the first
+ * topk_blocks slots INT32_MAX; nvalid[t] = min(nb_t, topk_blocks)
+ * (sglang PR #40352, Design: ragged top-k over the keys, rows with at most
+ * 2048 blocks keep everything, ids sorted ascending and INT32_MAX padded).
+ *
+ * keys as written by ci_score_dense_amax8 (same stride rules);
+ * blocks: int32 [rows][blocks_stride], blocks_stride >= topk_blocks;
+ * nvalid: int32 [rows].  1 <= topk_blocks <= 16384; max_len <= 393216.
+ */
+CI_API int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys,
+                      int64_t keys_stride, int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride,
+                      int32_t* nvalid, int32_t* dev_err, void* stream);
+
+/*
+ * Level two: a layer's top-k positions inside the candidate blocks.
+ *
+ * For every row t the candidate positions are s = 8 * blocks[t][i] + j,
+ * i < nvalid[t], j < 8, s < L_t, in ascending order (blocks must be ascending,
+ * as ci_publish_blocks writes them).  Each is scored with this layer's q, w
+ * and k_pool exactly as in ci_score_dense_amax8, and the topk best (ties:
+ * lower position first) are written ascending to out_pos[t * out_stride + i],
+ * i < topk, with -1 past min(topk, number of candidate positions)
+ * (sglang PR #40352, Design, "Level two": top-512 of the first valid_len
+ * columns, page transform to request-relative positions, -1 past
+ * min(512, valid_len)).  If out_score is not NULL, out_score[t*out_stride+i]
+ * receives the fp32 score of out_pos[...] (-inf where out_pos is -1).
+ *
+ * The source layer's own top-512 is this call on the source layer with the
+ * top max(topk_blocks, 513) blocks: every position of the dense top-512 lies
+ * in those blocks.
+ *
+ * blocks: int32 [rows][blocks_stride]; nvalid: int32 [rows], each
+ * 0 <= nvalid[t] <= max_blocks <= min(blocks_stride, 3072).
+ * 1 <= topk <= 2048, topk <= out_stride.
+ */
+CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
+                     int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                     int32_t layout, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                     const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
+                     int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
+                     void* stream);
+
+/* Human-readable name of a ci_status code (static storage). */
+CI_API const char* ci_strerror(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+CI_API int ci_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CI_H_ */

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and rejects
+bad arguments on the host (no GPU needed: these checks run before any CUDA
+call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ci.h")
+
+
+@pytest.fixture(scope="module")
+def ci():
+    from two_level_sparse_gb300 import build
+
+    if not os.path.exists(os.path.join(ROOT, "two_level_sparse_gb300", "libci.so")):
+        build.build()
+    from two_level_sparse_gb300 import ci as mod
+
+    return mod
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(ci_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_symbols() == sorted(
+        ["ci_publish_blocks", "ci_score_dense_amax8", "ci_select_sparse", "ci_strerror", "ci_version"])
+
+
+def test_library_exports_every_declared_symbol(ci):
+    lib = ctypes.CDLL(ci.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(ci.SIGNATURES) == set(declared_symbols())
+
+
+def test_status_names(ci):
+    assert ci.version() == 100
+    assert ci.strerror(0) == "ok"
+    for code in ci.CI_ERR:
+        assert ci.strerror(code) != "unknown status"
+
+
+P = ctypes.c_void_p(0x1000)  # never dereferenced: host checks fail first
+N = None
+
+
+def test_dense_host_checks(ci):
+    f = ci.lib.ci_score_dense_amax8
+    # rows == 0: nothing to do, even with null pointers
+    assert f(N, N, N, N, 1, N, 0, 1, 0, N, 0, 0, 0, N, 8, N, N) == 0
+    # null pointer
+    assert f(N, P, P, P, 1, P, 2, 1, 0, P, 2, 64, 0, P, 8, N, N) == -1
+    # bad layout
+    assert f(P, P, P, P, 1, P, 2, 1, 7, P, 2, 64, 0, P, 8, N, N) == -5
+    # decode needs one request per row
+    assert f(P, P, P, P, 1, P, 3, 1, 0, P, 2, 64, 0, P, 8, N, N) == -2
+    # prefill needs exactly one request
+    assert f(P, P, P, P, 1, P, 2, 1, 1, P, 2, 64, 0, P, 8, N, N) == -2
+    # max_len beyond the page table
+    assert f(P, P, P, P, 1, P, 2, 1, 0, P, 2, 65, 0, P, 16, N, N) == -2
+    # keys stride not a multiple of 8 / too short
+    assert f(P, P, P, P, 1, P, 2, 2, 0, P, 2, 128, 0, P, 12, N, N) == -2
+    assert f(P, P, P, P, 1, P, 2, 4, 0, P, 2, 256, 0, P, 8, N, N) == -2
+    # misaligned pool
+    assert f(P, P, P, ctypes.c_void_p(0x1001), 1, P, 2, 1, 0, P, 2, 64, 0, P, 8, N, N) == -3
+    # negative skip
+    assert f(P, P, P, P, 1, P, 2, 1, 0, P, 2, 64, -1, P, 8, N, N) == -4
+
+
+def test_publish_host_checks(ci):
+    f = ci.lib.ci_publish_blocks
+    assert f(N, 0, 0, N, 8, 16, N, 16, N, N, N) == 0
+    assert f(P, 2, 64, P, 8, 0, P, 16, P, N, N) == -4  # topk_blocks < 1
+    assert f(P, 2, 64, P, 8, 16, P, 15, P, N, N) == -2  # blocks stride < topk
+    assert f(P, 2, 64, N, 8, 16, P, 16, P, N, N) == -1
+    assert f(P, 2, 400000, P, 50000, 16, P, 16, P, N, N) == -4  # longer than supported
+    assert f(P, 2, 64, ctypes.c_void_p(0x1004), 8, 16, P, 16, P, N, N) == -3
+
+
+def test_select_host_checks(ci):
+    f = ci.lib.ci_select_sparse
+    ok_args = [P, P, P, P, 1, P, 2, 1, 0, P, 2, 64, P, 16, P, 16, 8, P, N, 8, N, N]
+    assert f(*ok_args[:10], 0, *ok_args[11:]) == 0  # rows == 0
+    bad = list(ok_args)
+    bad[16] = 0  # topk < 1
+    assert f(*bad) == -4
+    bad = list(ok_args)
+    bad[15] = 5000  # max_blocks too large
+    assert f(*bad) == -4
+    bad = list(ok_args)
+    bad[19] = 4  # out stride < topk
+    assert f(*bad) == -2
+    bad = list(ok_args)
+    bad[17] = N  # no output
+    assert f(*bad) == -1

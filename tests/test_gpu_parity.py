@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Small workloads are checked row by row in full; the five standard workloads
+run at full size in the same launch configuration the benchmark uses and are
+checked on sampled rows (every output of a sampled row: keys, published
+blocks, the source's own top-512 and the four consumers' top-512).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import ci_oracle as O
+from oracle import compare
+from two_level_sparse_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")
+
+
+@pytest.fixture(scope="module")
+def ci():
+    from two_level_sparse_gb300 import ci as mod
+
+    return mod
+
+
+def run_step(wl_cpu, device="cuda", with_scores=True, wl_dev=None):
+    from two_level_sparse_gb300.step import IndexerStep
+
+    step = IndexerStep(wl_dev if wl_dev is not None else wl_cpu.to(device), with_scores=with_scores)
+    step.run()
+    torch.cuda.synchronize()
+    return step
+
+
+def assert_ok(rep):
+    assert rep.ok, rep
+
+
+@needs_cuda
+def test_tiny_decode_config_all_rows(ci):
+    wl = synth.config_workload(0)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    rep = compare.check_step(wl, step.outputs_numpy())
+    assert_ok(rep)
+
+
+@needs_cuda
+@pytest.mark.parametrize("lens,K,P", [
+    ([0, 1, 7, 8, 9, 100, 2100, 20000], 128, 512),   # empty row, ragged tails, keep-all and selecting rows
+    ([5000, 5001, 4096, 4095, 65], 64, 40),           # small top-k, selection on every long row
+    ([1500, 3000], 600, 2048),                        # topk larger than every candidate set
+])
+def test_small_decode_all_rows(ci, lens, K, P):
+    wl = synth.make_workload("dec", synth.LAYOUT_DECODE, lens, topk_blocks=K, seed=101, topk=P)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+@needs_cuda
+@pytest.mark.parametrize("rows,base,K", [(7, 3000, 64), (4, 129, 8), (10, 2040, 200)])
+def test_small_prefill_all_rows(ci, rows, base, K):
+    # causal rows of one request; rows % 3 != 0 leaves a ragged last row group
+    lens = [base + i for i in range(rows)]
+    wl = synth.make_workload("pre", synth.LAYOUT_PREFILL, lens, topk_blocks=K, seed=202)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+@needs_cuda
+def test_duplicate_blocks_score_bit_identically(ci):
+    # every copy of a block must get bit-identical keys (the tie rule needs it)
+    wl = synth.make_workload("dup", synth.LAYOUT_DECODE, [4000, 3000], topk_blocks=16, seed=9, dup_frac=0.2)
+    step = run_step(wl)
+    keys = step.keys.cpu().numpy()
+    vals, scales = O.page_values_and_scales(wl.layers[0].k_pool.numpy())
+    pt = wl.page_table.numpy()
+    pairs = 0
+    for t, L in enumerate(wl.seq_len.tolist()):
+        sig = {}
+        for b in range(O.num_blocks(L) - 1):
+            p, o = pt[t, b // 8], (b % 8) * 8
+            sig.setdefault((vals[p, o:o + 8].tobytes(), scales[p, o:o + 8].tobytes()), []).append(b)
+        for group in sig.values():
+            if len(group) > 1:
+                pairs += 1
+                assert len({keys[t, b].tobytes() for b in group}) == 1
+    assert pairs > 0
+
+
+@needs_cuda
+def test_dense_keys_equal_sparse_rescoring_bitwise(ci):
+    # The sparse scorer reproduces the dense scorer's fp32 scores bit for bit,
+    # which the source's own top-512 through its top-(P+1) blocks relies on:
+    # with every block a candidate and topk >= L, select returns every position
+    # with its score, and each block's maximum must equal its dense key.
+    from two_level_sparse_gb300.step import IndexerStep
+
+    lens = [2000, 2001, 2002, 2040]
+    wl = synth.make_workload("lemma", synth.LAYOUT_PREFILL, lens, topk_blocks=64, seed=5)
+    dev = wl.to("cuda")
+    step = IndexerStep(dev)
+    step.run()
+    rows, L = wl.rows, max(lens)
+    nb = O.num_blocks(L)
+    allb = torch.arange(nb, dtype=torch.int32, device="cuda").repeat(rows, 1).contiguous()
+    nv = torch.tensor([O.num_blocks(x) for x in lens], dtype=torch.int32, device="cuda")
+    pos = torch.empty(rows, 2048, dtype=torch.int32, device="cuda")
+    sc = torch.empty(rows, 2048, dtype=torch.float32, device="cuda")
+    src = dev.layers[0]
+    ci.ci_select_sparse(src.q_fp4, src.q_sf, src.w, src.k_pool, dev.page_table, dev.layout, dev.seq_len, L, allb, nv,
+                        nb, 2048, pos, sc)
+    torch.cuda.synchronize()
+    keys = step.keys.cpu().numpy()
+    pos, sc = pos.cpu().numpy(), sc.cpu().numpy()
+    for t, Lt in enumerate(lens):
+        assert pos[t, :Lt].tolist() == list(range(Lt)) and np.all(pos[t, Lt:] == -1)
+        for b in range(O.num_blocks(Lt) - 1):
+            assert keys[t, b].tobytes() == sc[t, 8 * b:8 * b + 8].max().tobytes(), (t, b)
+
+
+@needs_cuda
+def test_device_error_flags_bad_page_without_fault(ci):
+    wl = synth.make_workload("bad", synth.LAYOUT_DECODE, [3000, 2000], topk_blocks=64, seed=3)
+    dev = wl.to("cuda")
+    dev.page_table[1, 3] = 10**6  # outside the pool: the kernel must skip it and flag
+    from two_level_sparse_gb300.step import IndexerStep
+
+    step = IndexerStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) & ci.DEVERR_PAGE
+    # row 0 is untouched by the corruption
+    rep = compare.check_step(wl, step.outputs_numpy(), rows=[0])
+    assert_ok(rep)
+
+
+@needs_cuda
+def test_device_error_flags_length_above_max(ci):
+    wl = synth.make_workload("len", synth.LAYOUT_DECODE, [3000, 2000], topk_blocks=64, seed=4)
+    dev = wl.to("cuda")
+    keys = torch.zeros(2, 512, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    src = dev.layers[0]
+    # claim max_len 2500 although row 0 has 3000 positions
+    ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, dev.page_table, dev.layout, dev.seq_len, 2500, 8,
+                            keys, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ci.DEVERR_LEN
+
+
+@needs_cuda
+def test_empty_batch_is_a_no_op(ci):
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    u8 = torch.empty(0, 64, 64, dtype=torch.uint8, device="cuda")
+    pool = torch.zeros(1, synth.PAGE_BYTES, dtype=torch.uint8, device="cuda")
+    pt = torch.zeros(1, 1, dtype=torch.int32, device="cuda")
+    keys = torch.empty(0, 8, dtype=torch.float32, device="cuda")
+    ci.ci_score_dense_amax8(u8, torch.empty(0, 64, 4, dtype=torch.uint8, device="cuda"),
+                            torch.empty(0, 64, dtype=torch.float32, device="cuda"), pool, pt, 1, e, 0, 0, keys)
+    torch.cuda.synchronize()
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+SAMPLES = {
+    1: [0, 1, 31, 62, 63],
+    2: None,  # chosen below: short (keep-all) and long rows
+    3: [0, 1, 2, 2047, 4093, 4094, 4095],
+    4: [0, 1, 2, 5000, 9999, 16381, 16382, 16383],
+}
+
+
+@needs_cuda
+@pytest.mark.parametrize("cid", [1, 2, 3, 4])
+def test_full_size_config_sampled_rows(ci, cid):
+    wl_dev = synth.config_workload(cid, device="cuda")
+    step = run_step(None, wl_dev=wl_dev)
+    assert int(step.dev_err.item()) == 0
+    if cid == 2:
+        lens = wl_dev.seq_len.cpu()
+        short = [int(i) for i in torch.nonzero(lens <= 16384).flatten()[:2]]
+        long = [int(i) for i in torch.nonzero(lens > 131072).flatten()[:3]]
+        rows = short + long + [int(torch.argmax(lens))]
+    else:
+        rows = SAMPLES[cid]
+    sub = subset_workload(wl_dev, rows)
+    out = step.outputs_numpy()
+    sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
+    assert_ok(compare.check_step(sub, sub_out))
+
+
+def subset_workload(wl_dev, rows):
+    """The sampled rows' operands on the CPU (the whole pool comes along)."""
+    idx = torch.tensor(rows, dtype=torch.long, device=wl_dev.seq_len.device)
+    layers = [synth.Layer(l.q_fp4[idx].cpu(), l.q_sf[idx].cpu(), l.w[idx].cpu(), l.k_pool.cpu()) for l in wl_dev.layers]
+    pt = wl_dev.page_table[idx].cpu() if wl_dev.layout == synth.LAYOUT_DECODE else wl_dev.page_table.cpu()
+    return synth.Workload(wl_dev.name, wl_dev.layout, wl_dev.seq_len[idx].cpu(), pt, layers, wl_dev.topk_blocks,
+                          wl_dev.topk)

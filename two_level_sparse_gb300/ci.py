@@ -1,0 +1,139 @@
+"""ctypes binding of libci.so (include/ci.h), same entry-point names.
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current torch stream becomes the cudaStream_t, and a non-zero status becomes a
+``CIError``.  Every step of the computation runs in the library's kernels.
+Importing this module fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libci.so")
+
+CI_OK = 0
+CI_ERR = {
+    -1: "CI_ERR_NULL",
+    -2: "CI_ERR_SHAPE",
+    -3: "CI_ERR_ALIGN",
+    -4: "CI_ERR_RANGE",
+    -5: "CI_ERR_UNSUPPORTED",
+    -6: "CI_ERR_CUDA",
+}
+LAYOUT_DECODE = 0
+LAYOUT_PREFILL = 1
+DEVERR_LEN, DEVERR_PAGE, DEVERR_BLOCK, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+SIGNATURES = {
+    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
+    "ci_publish_blocks": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P, _P],
+    "ci_select_sparse": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _I32, _I32, _P, _I64, _P, _I32, _I32, _P, _P,
+                         _I64, _P, _P],
+    "ci_strerror": [ctypes.c_int],
+    "ci_version": [],
+}
+
+
+class CIError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {status} ({CI_ERR.get(status, '?')}: {strerror(status)})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, argtypes in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argtypes
+        fn.restype = ctypes.c_char_p if name == "ci_strerror" else ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def strerror(status: int) -> str:
+    return lib.ci_strerror(status).decode()
+
+
+def version() -> int:
+    return lib.ci_version()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != CI_OK:
+        raise CIError(fn, status)
+
+
+def _expect(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def ci_score_dense_amax8(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, skip_le_blocks, keys,
+                         dev_err=None, stream=None):
+    """Block keys of the source layer (see include/ci.h)."""
+    for t, d, n in ((q_fp4, torch.uint8, "q_fp4"), (q_sf, torch.uint8, "q_sf"), (w, torch.float32, "w"),
+                    (k_pool, torch.uint8, "k_pool"), (page_table, torch.int32, "page_table"),
+                    (seq_len, torch.int32, "seq_len"), (keys, torch.float32, "keys")):
+        _expect(t, d, n)
+    rows = int(seq_len.shape[0])
+    _check("ci_score_dense_amax8", lib.ci_score_dense_amax8(
+        _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), _ptr(page_table),
+        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _ptr(seq_len), rows, int(max_len),
+        int(skip_le_blocks), _ptr(keys), int(keys.stride(0)) if keys.dim() == 2 else 0, _ptr(dev_err),
+        _stream(stream)))
+
+
+def ci_publish_blocks(seq_len, max_len, keys, topk_blocks, blocks, nvalid, dev_err=None, stream=None):
+    """Each row's candidate blocks, ascending, INT32_MAX padded (see include/ci.h)."""
+    _expect(seq_len, torch.int32, "seq_len")
+    _expect(keys, torch.float32, "keys")
+    _expect(blocks, torch.int32, "blocks")
+    _expect(nvalid, torch.int32, "nvalid")
+    rows = int(seq_len.shape[0])
+    _check("ci_publish_blocks", lib.ci_publish_blocks(
+        _ptr(seq_len), rows, int(max_len), _ptr(keys), int(keys.stride(0)), int(topk_blocks), _ptr(blocks),
+        int(blocks.stride(0)), _ptr(nvalid), _ptr(dev_err), _stream(stream)))
+
+
+def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, blocks, nvalid, max_blocks, topk,
+                     out_pos, out_score=None, dev_err=None, stream=None):
+    """A layer's top-k positions inside the candidate blocks (see include/ci.h)."""
+    for t, d, n in ((q_fp4, torch.uint8, "q_fp4"), (q_sf, torch.uint8, "q_sf"), (w, torch.float32, "w"),
+                    (k_pool, torch.uint8, "k_pool"), (page_table, torch.int32, "page_table"),
+                    (seq_len, torch.int32, "seq_len"), (blocks, torch.int32, "blocks"),
+                    (nvalid, torch.int32, "nvalid"), (out_pos, torch.int32, "out_pos")):
+        _expect(t, d, n)
+    if out_score is not None:
+        _expect(out_score, torch.float32, "out_score")
+    rows = int(seq_len.shape[0])
+    _check("ci_select_sparse", lib.ci_select_sparse(
+        _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), _ptr(page_table),
+        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _ptr(seq_len), rows, int(max_len),
+        _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(topk), _ptr(out_pos),
+        _ptr(out_score), int(out_pos.stride(0)), _ptr(dev_err), _stream(stream)))

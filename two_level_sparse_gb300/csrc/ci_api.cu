@@ -1,0 +1,154 @@
+// The C ABI declared in include/ci.h: host-side argument checks, then one
+// kernel launch per call.  No allocation, no synchronization.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/ci.h"
+#include "ci_internal.h"
+
+namespace ci {
+
+int device_sm_count() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (counts[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = n > 0 ? n : 1;
+  }
+  return counts[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+cudaError_t make_pool_tmap(CUtensorMap* map, const uint8_t* k_pool, int64_t num_pages, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(CI_DIM), static_cast<cuuint64_t>(CI_PAGE),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(CI_DIM), static_cast<cuuint64_t>(CI_PAGE_BYTES)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(CI_DIM), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(k_pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace ci
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by the two scoring entry points.
+int check_pool(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool, int64_t num_pages,
+               const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout, const int32_t* seq_len,
+               int32_t rows, int32_t max_len) {
+  if (rows < 0 || max_len < 0 || num_pages < 0 || num_req < 0 || max_pages < 0) return CI_ERR_SHAPE;
+  if (layout != CI_LAYOUT_DECODE && layout != CI_LAYOUT_PREFILL) return CI_ERR_UNSUPPORTED;
+  if (rows == 0) return CI_OK;
+  if (!q_fp4 || !q_sf || !w || !k_pool || !page_table || !seq_len) return CI_ERR_NULL;
+  if (layout == CI_LAYOUT_DECODE && num_req != rows) return CI_ERR_SHAPE;
+  if (layout == CI_LAYOUT_PREFILL && num_req != 1) return CI_ERR_SHAPE;
+  if (static_cast<int64_t>(max_len) > static_cast<int64_t>(max_pages) * CI_PAGE) return CI_ERR_SHAPE;
+  if (num_pages < 1 || num_pages > INT32_MAX) return CI_ERR_RANGE;
+  if (!aligned(k_pool, 16) || !aligned(q_fp4, 8) || !aligned(q_sf, 4) || !aligned(w, 8)) return CI_ERR_ALIGN;
+  return CI_OK;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? CI_OK : CI_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int ci_version(void) { return 100; }
+
+const char* ci_strerror(int status) {
+  switch (status) {
+    case CI_OK: return "ok";
+    case CI_ERR_NULL: return "a required pointer is NULL";
+    case CI_ERR_SHAPE: return "inconsistent sizes or strides";
+    case CI_ERR_ALIGN: return "a pointer or stride breaks an alignment rule";
+    case CI_ERR_RANGE: return "a size is out of its supported range";
+    case CI_ERR_UNSUPPORTED: return "a valid request this build does not implement";
+    case CI_ERR_CUDA: return "a CUDA call failed";
+    default: return "unknown status";
+  }
+}
+
+int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
+                         int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                         int32_t layout, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                         int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err, void* stream) {
+  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, seq_len, rows,
+                      max_len);
+  if (st != CI_OK) return st;
+  if (skip_le_blocks < 0) return CI_ERR_RANGE;
+  if (rows == 0) return CI_OK;
+  if (!keys) return CI_ERR_NULL;
+  if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
+  if (!aligned(keys, 16)) return CI_ERR_ALIGN;
+  ci::DenseArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, seq_len, rows, max_len, dev_err},
+                  skip_le_blocks,
+                  keys,
+                  keys_stride};
+  return launched(ci::launch_dense_amax8(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys, int64_t keys_stride,
+                      int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride, int32_t* nvalid, int32_t* dev_err,
+                      void* stream) {
+  if (rows < 0 || max_len < 0) return CI_ERR_SHAPE;
+  if (topk_blocks < 1 || topk_blocks > 16384) return CI_ERR_RANGE;
+  if (max_len > 393216) return CI_ERR_RANGE;
+  if (rows == 0) return CI_OK;
+  if (!seq_len || !keys || !blocks || !nvalid) return CI_ERR_NULL;
+  if (blocks_stride < topk_blocks) return CI_ERR_SHAPE;
+  if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
+  if (!aligned(keys, 16)) return CI_ERR_ALIGN;
+  ci::PublishArgs a{seq_len, rows, max_len, keys, keys_stride, topk_blocks, blocks, blocks_stride, nvalid, dev_err};
+  return launched(ci::launch_publish(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
+                     int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
+                     const int32_t* seq_len, int32_t rows, int32_t max_len, const int32_t* blocks,
+                     int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks, int32_t topk, int32_t* out_pos,
+                     float* out_score, int64_t out_stride, int32_t* dev_err, void* stream) {
+  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, seq_len, rows,
+                      max_len);
+  if (st != CI_OK) return st;
+  if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
+  if (max_blocks < 0 || max_blocks > 3072) return CI_ERR_RANGE;
+  if (rows == 0) return CI_OK;
+  if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
+  if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;
+  ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, seq_len, rows, max_len, dev_err},
+                   blocks,
+                   blocks_stride,
+                   nvalid,
+                   max_blocks,
+                   topk,
+                   out_pos,
+                   out_score,
+                   out_stride};
+  return launched(ci::launch_select(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

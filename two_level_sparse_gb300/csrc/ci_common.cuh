@@ -1,0 +1,231 @@
+// Device helpers shared by the scoring, publishing and selection kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+
+namespace ci {
+
+constexpr int kHeads = 64;
+constexpr int kDim = 128;
+constexpr int kBlock = 8;
+constexpr int kPage = 64;
+constexpr int kPageValueBytes = kPage * kDim;          // 8192
+constexpr int kPageBytes = kPageValueBytes + kPage * 4;  // 8448
+constexpr int kTileM = 128;                            // positions per MMA tile
+constexpr uint32_t kDevErrLen = 1u, kDevErrPage = 2u, kDevErrBlock = 4u, kDevErrTimeout = 8u;
+
+__device__ __forceinline__ void report(int32_t* dev_err, uint32_t bits) {
+  if (dev_err != nullptr) atomicOr(reinterpret_cast<unsigned int*>(dev_err), bits);
+}
+
+// Byte offset of (row r, byte kb) inside a K-major tile of 128-byte rows in the
+// 128-byte swizzle layout (8-row atoms of 1024 B; the 16-byte chunk index is
+// XOR-ed with the row index inside the atom).
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t kb) {
+  return (r >> 3) * 1024u + (r & 7u) * 128u + ((((kb >> 4) ^ (r & 7u)) << 4) | (kb & 15u));
+}
+
+// e2m1 code (sign bit 3) -> e4m3 byte of the same value.  Every e2m1 value
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6} is exact in e4m3.
+__device__ __forceinline__ uint32_t e2m1_to_e4m3(uint32_t code) {
+  constexpr uint64_t kMag = 0x4C4844403C383000ull;  // bytes for magnitudes 0..7
+  return static_cast<uint32_t>((kMag >> ((code & 7u) * 8u)) & 0xFFu) | ((code & 8u) << 4);
+}
+
+// 8 packed MXFP4 bytes (16 codes, element 2i in the low nibble) -> 16 e4m3 bytes.
+__device__ __forceinline__ uint4 widen_fp4x16(uint2 in) {
+  uint32_t o[4];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t v = half ? in.y : in.x;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t b = v >> (16 * q);  // two bytes -> four codes
+      o[half * 2 + q] = e2m1_to_e4m3(b & 0xF) | (e2m1_to_e4m3((b >> 4) & 0xF) << 8) |
+                        (e2m1_to_e4m3((b >> 8) & 0xF) << 16) | (e2m1_to_e4m3((b >> 12) & 0xF) << 24);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Warp-uniform bounded wait: lane 0 waits (giving up on abort or timeout), the
+// verdict is broadcast, and on success every lane observes the completed phase
+// itself (an immediate try_wait) so that each has acquire ordering.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) mbar_wait(bar, parity, nullptr);
+  return ok;
+}
+
+// ---------------------------------------------------------------- score epilogue
+// Head-weighted ReLU reduction of one (row, position) pair from its 64 fp32
+// accumulator columns, delivered in two halves of 32.  Eight partial sums, two
+// per packed fp32x2 FMA, combined in a fixed tree: every kernel that scores a
+// position uses this function, so identical K vectors give identical scores.
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+
+// acc[4]: partial sums; x: 32 accumulator words for heads [32*half, 32*half+32);
+// w2: the 16 packed weight pairs of those heads.
+__device__ __forceinline__ void head_reduce_half(uint64_t (&acc)[4], const uint32_t (&x)[32],
+                                                 const uint64_t* w2) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float r0 = fmaxf(__uint_as_float(x[2 * j]), 0.0f);
+    const float r1 = fmaxf(__uint_as_float(x[2 * j + 1]), 0.0f);
+    ffma2(acc[j & 3], w2[j], pack2(r0, r1));
+  }
+}
+__device__ __forceinline__ float head_reduce_finish(const uint64_t (&acc)[4]) {
+  const float2 a = unpack2(acc[0]), b = unpack2(acc[1]), c = unpack2(acc[2]), d = unpack2(acc[3]);
+  return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+}
+
+// ---------------------------------------------------------------- ordering keys
+// Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 maps
+// like +0.  Every finite score and -inf map above 0, which marks "no entry".
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_inv(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ---------------------------------------------------------------- block top-k
+struct TopkShared {
+  uint32_t hist[256];
+  uint32_t warp_gt[32];
+  uint32_t warp_eq[32];
+  uint32_t sel_digit, sel_remaining, sel_match;
+};
+
+// Selects the k largest of the uint32 keys sk[0..n) (k <= n), ties toward the
+// lower index, and calls emit(rank, index, key) once per selected entry with
+// rank = its place in ascending index order.  Radix select on 8-bit digits
+// from the top, stopping as soon as the threshold digit's bucket is taken
+// whole, then an ordered compaction.  Executed by `nthreads` threads (a
+// multiple of 32, thread ids 0..nthreads-1) that sync on named barrier bar_id.
+template <class Emit>
+__device__ __forceinline__ void block_topk(const uint32_t* sk, int n, int k, TopkShared& sh, int tid, int nthreads,
+                                           int bar_id, Emit emit) {
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += nthreads) sh.hist[i] = 0;
+    named_sync(bar_id, nthreads);
+    for (int i = tid; i < n; i += nthreads) {
+      const uint32_t u = sk[i];
+      if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & 255u], 1u);
+    }
+    named_sync(bar_id, nthreads);
+    if (tid < 32) {
+      uint32_t c[8], lane_sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sh.hist[tid * 8 + j];
+        lane_sum += c[j];
+      }
+      uint32_t suffix = lane_sum;  // sum over lanes >= tid
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, suffix, off);
+        if (tid + off < 32) suffix += v;
+      }
+      const uint32_t above = suffix - lane_sum;  // keys whose digit lies above this lane's bins
+      if (above < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= suffix) {
+        uint32_t acc = above;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+          if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
+            sh.sel_digit = tid * 8 + j;
+            sh.sel_remaining = remaining - acc;
+            sh.sel_match = c[j];
+            break;
+          }
+          acc += c[j];
+        }
+      }
+    }
+    named_sync(bar_id, nthreads);
+    const uint32_t d = sh.sel_digit;
+    remaining = static_cast<int>(sh.sel_remaining);
+    const uint32_t match = sh.sel_match;
+    prefix |= d << shift;
+    mask |= 0xFFu << shift;
+    if (match == static_cast<uint32_t>(remaining)) break;  // the whole bucket is taken
+  }
+  const int need_eq = remaining;
+  // ordered compaction: warps own contiguous segments
+  const int nwarps = nthreads >> 5, wid = tid >> 5, lane = tid & 31;
+  const int seg = ((n + nwarps - 1) / nwarps + 31) & ~31;
+  const int begin = min(n, wid * seg), end = min(n, begin + seg);
+  uint32_t gt = 0, eq = 0;
+  for (int i = begin + lane; i < end; i += 32) {
+    const uint32_t m = sk[i] & mask;
+    gt += m > prefix;
+    eq += m == prefix;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, off);
+    eq += __shfl_xor_sync(0xffffffffu, eq, off);
+  }
+  if (lane == 0) {
+    sh.warp_gt[wid] = gt;
+    sh.warp_eq[wid] = eq;
+  }
+  named_sync(bar_id, nthreads);
+  uint32_t gt_before = 0, eq_before = 0;
+  for (int w = 0; w < wid; ++w) {
+    gt_before += sh.warp_gt[w];
+    eq_before += sh.warp_eq[w];
+  }
+  const uint32_t lt = lanemask_lt();
+  for (int base = begin; base < end; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < end;
+    const uint32_t u = valid ? sk[i] : 0u;
+    const uint32_t m = u & mask;
+    const bool is_gt = valid && m > prefix;
+    const bool is_eq = valid && m == prefix;
+    const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
+    const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t eq_rank = eq_before + __popc(be & lt);
+    if (is_gt || (is_eq && eq_rank < static_cast<uint32_t>(need_eq))) {
+      const uint32_t rank = gt_before + __popc(bg & lt) + min(eq_rank, static_cast<uint32_t>(need_eq));
+      emit(static_cast<int>(rank), i, u);
+    }
+    gt_before += __popc(bg);
+    eq_before += __popc(be);
+  }
+  named_sync(bar_id, nthreads);  // sh is reused by the caller's next selection
+}
+
+}  // namespace ci

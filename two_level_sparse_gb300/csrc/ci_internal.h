@@ -1,0 +1,68 @@
+// Host-side interface between the C ABI (ci_api.cu) and the kernel launchers.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ci {
+
+struct PoolArgs {
+  const uint8_t* q_fp4;
+  const uint8_t* q_sf;
+  const float* w;
+  const uint8_t* k_pool;
+  int64_t num_pages;
+  const int32_t* page_table;
+  int32_t max_pages;
+  int32_t layout;  // 0 decode (row t = request t), 1 prefill (one request)
+  const int32_t* seq_len;
+  int32_t rows;
+  int32_t max_len;
+  int32_t* dev_err;
+};
+
+struct DenseArgs {
+  PoolArgs p;
+  int32_t skip_le_blocks;
+  float* keys;
+  int64_t keys_stride;
+};
+
+struct PublishArgs {
+  const int32_t* seq_len;
+  int32_t rows;
+  int32_t max_len;
+  const float* keys;
+  int64_t keys_stride;
+  int32_t topk_blocks;
+  int32_t* blocks;
+  int64_t blocks_stride;
+  int32_t* nvalid;
+  int32_t* dev_err;
+};
+
+struct SelectArgs {
+  PoolArgs p;
+  const int32_t* blocks;
+  int64_t blocks_stride;
+  const int32_t* nvalid;
+  int32_t max_blocks;
+  int32_t topk;
+  int32_t* out_pos;
+  float* out_score;
+  int64_t out_stride;
+};
+
+// Each returns a cudaError_t from the launch (cudaSuccess when enqueued).
+cudaError_t launch_dense_amax8(const DenseArgs& a, cudaStream_t stream);
+cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
+
+// Shared host helpers (ci_api.cu).
+int device_sm_count();
+// Tensor map over the value bytes of a paged index-K pool viewed as
+// [num_pages][64 positions][128 bytes], 128-byte swizzle, box of `box_rows`
+// positions of one page.
+cudaError_t make_pool_tmap(CUtensorMap* map, const uint8_t* k_pool, int64_t num_pages, int box_rows);
+
+}  // namespace ci

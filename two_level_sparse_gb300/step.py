@@ -1,0 +1,87 @@
+"""One indexer step through the C ABI: the source layer's dense keys and
+published blocks, then every layer's top-k positions.
+
+Call sequence (sglang PR #40352, Design: the source computes its dense scores,
+publishes its candidate blocks and runs its own top-512; each consumer selects
+within the published blocks):
+
+  ci_score_dense_amax8(source)                   keys, rows with > K blocks
+  ci_publish_blocks(keys, K')                    the source's own candidates
+  ci_publish_blocks(keys, K)        (if K' != K) the consumers' candidates
+  ci_select_sparse(source, K' blocks)            the source's top-P
+  ci_select_sparse(consumer j, K blocks)         each consumer's top-P
+
+with K' = max(K, P + 1): every position of the dense top-P lies in the top
+P + 1 blocks by key (the newest block's key is +inf and every other block that
+outranks a position's block holds a distinct higher-scoring position), so the
+source's top-P over its top-K' blocks is its dense top-P.
+
+This module only allocates the output buffers (torch device memory) and
+marshals arguments; all computation runs in libci.so.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ci
+
+
+class IndexerStep:
+    def __init__(self, wl, with_scores: bool = False):
+        dev = wl.seq_len.device
+        self.wl = wl
+        self.rows = wl.rows
+        self.max_len = wl.max_len
+        self.K = wl.topk_blocks
+        self.P = wl.topk
+        self.Kp = max(self.K, self.P + 1)
+        nb_max = (self.max_len + 7) // 8
+        stride = max(8, (nb_max + 7) // 8 * 8)
+        i32 = torch.int32
+        self.keys = torch.empty(self.rows, stride, dtype=torch.float32, device=dev)
+        self.blocks_src = torch.empty(self.rows, self.Kp, dtype=i32, device=dev)
+        self.nvalid_src = torch.empty(self.rows, dtype=i32, device=dev)
+        if self.Kp == self.K:
+            self.blocks, self.nvalid = self.blocks_src, self.nvalid_src
+        else:
+            self.blocks = torch.empty(self.rows, self.K, dtype=i32, device=dev)
+            self.nvalid = torch.empty(self.rows, dtype=i32, device=dev)
+        nl = len(wl.layers)
+        self.pos = torch.empty(nl, self.rows, self.P, dtype=i32, device=dev)
+        self.score = torch.empty(nl, self.rows, self.P, dtype=torch.float32, device=dev) if with_scores else None
+        self.dev_err = torch.zeros(1, dtype=i32, device=dev)
+
+    def launches(self) -> int:
+        """Kernels one run() enqueues."""
+        return 1 + (1 if self.Kp == self.K else 2) + len(self.wl.layers)
+
+    def run(self, stream=None, skip_dense=False):
+        """Enqueue the step on `stream` (default: torch's current stream).
+        ``skip_dense`` leaves out the first call, for callers that enqueue it
+        themselves (the benchmark times it on its own)."""
+        wl = self.wl
+        src = wl.layers[0]
+        common = dict(page_table=wl.page_table, layout=wl.layout, seq_len=wl.seq_len, max_len=self.max_len,
+                      dev_err=self.dev_err, stream=stream)
+        if not skip_dense:
+            ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, skip_le_blocks=self.K, keys=self.keys,
+                                    **common)
+        ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.Kp, self.blocks_src, self.nvalid_src,
+                             dev_err=self.dev_err, stream=stream)
+        if self.Kp != self.K:
+            ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
+                                 dev_err=self.dev_err, stream=stream)
+        for j, layer in enumerate(wl.layers):
+            blocks, nvalid, mb = (self.blocks_src, self.nvalid_src, self.Kp) if j == 0 else (self.blocks,
+                                                                                            self.nvalid, self.K)
+            ci.ci_select_sparse(layer.q_fp4, layer.q_sf, layer.w, layer.k_pool, blocks=blocks, nvalid=nvalid,
+                                max_blocks=mb, topk=self.P, out_pos=self.pos[j],
+                                out_score=None if self.score is None else self.score[j], **common)
+
+    def outputs_numpy(self):
+        out = dict(keys=self.keys.cpu().numpy(), blocks=self.blocks.cpu().numpy(), nvalid=self.nvalid.cpu().numpy(),
+                   blocks_src=self.blocks_src.cpu().numpy(), nvalid_src=self.nvalid_src.cpu().numpy(),
+                   pos=self.pos.cpu().numpy())
+        if self.score is not None:
+            out["score"] = self.score.cpu().numpy()
+        return out
