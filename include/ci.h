@@ -33,7 +33,8 @@
  *  - Index-K pool: k_pool uint8 [num_pages][8448].  Page p holds 64 positions:
  *    bytes [0, 8192) are their FP8 e4m3 vectors (128 bytes each), bytes
  *    [8192, 8448) their fp32 scales (little endian).  The scale multiplies the
- *    decoded vector.  k_pool must be 16-byte aligned.
+ *    decoded vector.  k_pool, q_sf and w must be 16-byte aligned, q_fp4 8-byte
+ *    aligned.
  *  - Page table: page_table int32 [num_req][max_pages]; logical page j of a
  *    request lives in physical page page_table[req][j].  Position s of a row
  *    is slot s % 64 of logical page s / 64.
@@ -154,7 +155,7 @@ CI_API int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_l
  * in those blocks.
  *
  * blocks: int32 [rows][blocks_stride]; nvalid: int32 [rows], each
- * 0 <= nvalid[t] <= max_blocks <= min(blocks_stride, 3072).
+ * 0 <= nvalid[t] <= max_blocks <= min(blocks_stride, 2176).
  * 1 <= topk <= 2048, topk <= out_stride.
  */
 CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,

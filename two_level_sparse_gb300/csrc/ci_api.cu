@@ -67,7 +67,7 @@ int check_pool(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const 
   if (layout == CI_LAYOUT_PREFILL && num_req != 1) return CI_ERR_SHAPE;
   if (static_cast<int64_t>(max_len) > static_cast<int64_t>(max_pages) * CI_PAGE) return CI_ERR_SHAPE;
   if (num_pages < 1 || num_pages > INT32_MAX) return CI_ERR_RANGE;
-  if (!aligned(k_pool, 16) || !aligned(q_fp4, 8) || !aligned(q_sf, 4) || !aligned(w, 8)) return CI_ERR_ALIGN;
+  if (!aligned(k_pool, 16) || !aligned(q_fp4, 8) || !aligned(q_sf, 16) || !aligned(w, 16)) return CI_ERR_ALIGN;
   return CI_OK;
 }
 
@@ -135,7 +135,7 @@ int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, 
                       max_len);
   if (st != CI_OK) return st;
   if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
-  if (max_blocks < 0 || max_blocks > 3072) return CI_ERR_RANGE;
+  if (max_blocks < 0 || max_blocks > 2176) return CI_ERR_RANGE;
   if (rows == 0) return CI_OK;
   if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
   if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;

@@ -63,37 +63,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // ---------------------------------------------------------------- score epilogue
 // Head-weighted ReLU reduction of one (row, position) pair from its 64 fp32
-// accumulator columns, delivered in two halves of 32.  Eight partial sums, two
-// per packed fp32x2 FMA, combined in a fixed tree: every kernel that scores a
-// position uses this function, so identical K vectors give identical scores.
-__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 unpack2(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return make_float2(lo, hi);
-}
-
-// acc[4]: partial sums; x: 32 accumulator words for heads [32*half, 32*half+32);
-// w2: the 16 packed weight pairs of those heads.
-__device__ __forceinline__ void head_reduce_half(uint64_t (&acc)[4], const uint32_t (&x)[32],
-                                                 const uint64_t* w2) {
+// accumulator columns, delivered in two halves of 32: eight partial sums
+// (head h feeds partial h % 8), combined in a fixed tree.  Every kernel that
+// scores a position uses this function, so identical K vectors give
+// bit-identical scores wherever they are scored.
+__device__ __forceinline__ void head_reduce_half(float (&acc)[8], const uint32_t (&x)[32], const float* w) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float r0 = fmaxf(__uint_as_float(x[2 * j]), 0.0f);
-    const float r1 = fmaxf(__uint_as_float(x[2 * j + 1]), 0.0f);
-    ffma2(acc[j & 3], w2[j], pack2(r0, r1));
-  }
+  for (int j = 0; j < 32; ++j) acc[j & 7] = fmaf(w[j], fmaxf(__uint_as_float(x[j]), 0.0f), acc[j & 7]);
 }
-__device__ __forceinline__ float head_reduce_finish(const uint64_t (&acc)[4]) {
-  const float2 a = unpack2(acc[0]), b = unpack2(acc[1]), c = unpack2(acc[2]), d = unpack2(acc[3]);
-  return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+__device__ __forceinline__ float head_reduce_finish(const float (&acc)[8]) {
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 // ---------------------------------------------------------------- ordering keys

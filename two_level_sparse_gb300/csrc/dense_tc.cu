@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t issued = 0;              // TMA thread: tiles whose loads were issued
   const int epi = warp >= kEpiWarp0 ? (warp - kEpiWarp0) >> 2 : -1;  // epilogue warpgroup
   const int quad = warp & 3;
-  uint64_t w2[32];
+  float w[kHeads];
 
   while (remaining > 0 && g < num_groups) {
     const int glen = group_len(a, g, geo.R);
@@ -231,11 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       row = geo.R == 3 ? g * 3 + epi : g;
       if (row < a.p.rows) {
         rlen = max(scored_len(a, row), 0);
-        const float2* wp = reinterpret_cast<const float2*>(a.p.w + static_cast<int64_t>(row) * kHeads);
+        const float4* wp = reinterpret_cast<const float4*>(a.p.w + static_cast<int64_t>(row) * kHeads);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 v = wp[j];
-          w2[j] = pack2(v.x, v.y);
+        for (int j = 0; j < 16; ++j) {
+          const float4 v = wp[j];
+          w[4 * j] = v.x;
+          w[4 * j + 1] = v.y;
+          w[4 * j + 2] = v.z;
+          w[4 * j + 3] = v.w;
         }
       }
     }
@@ -322,15 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint64_t part[4] = {0, 0, 0, 0};
+        float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint32_t x[32];
         const uint32_t taddr = tmem_addr(tbase, 32 * quad, acc * geo.N + col0);
         tmem_ld32(taddr, x);
         tmem_ld_wait();
-        head_reduce_half(part, x, w2);
+        head_reduce_half(part, x, w);
         tmem_ld32(taddr + 32, x);
         tmem_ld_wait();
-        head_reduce_half(part, x, w2 + 16);
+        head_reduce_half(part, x, w + 32);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.t_empty[acc]);

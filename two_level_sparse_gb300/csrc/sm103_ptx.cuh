@@ -49,17 +49,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when
-// `*abort` becomes non-zero or after `timeout_ns` of wall-clock time.
+// `*abort` becomes non-zero or after `timeout_ns` of wall-clock time.  After
+// the first probe the thread sleeps inside the barrier (suspend-time hint)
+// rather than spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity);
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
@@ -82,6 +83,33 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// Classic asynchronous global -> shared copies of 16 bytes (L2 only), grouped
+// per thread with commit/wait.  The writes are generic-proxy writes: a thread
+// that has waited for its groups must fence.proxy.async before the tensor
+// core may read them.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Bounded wait with a suspend-time hint, so a waiting thread sleeps in the
+// barrier instead of spinning through the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(200000u)
+      : "memory");
+  return ok != 0;
 }
 
 // ---------------------------------------------------------------- tensor memory
@@ -185,6 +213,22 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
+}
+
+// Copy 32 lanes x 128 bits (4 columns) from shared memory into tensor memory,
+// replicated into all four lane quadrants.  The source is 512 contiguous bytes:
+// lane l receives bytes [16 l, 16 l + 16).  Ordered with the tcgen05.mma
+// instructions the same thread issues afterwards.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;   // leading byte offset
+  d |= static_cast<uint64_t>(128u >> 4) << 32;  // stride between 8-row groups
+  d |= static_cast<uint64_t>(1u) << 46;         // version
+  return d;                                      // no swizzle
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
