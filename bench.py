@@ -103,13 +103,13 @@ def algorithmic_counts(wl):
     """FLOPs of the dense pass and bytes of index-K it must read.
 
     Dense scorer: 2 * H * D flops per (row, position) over rows with more than
-    K blocks.  Bytes: 132 per position of K (128 e4m3 + 4-byte scale) read
+    min(K, P + 1) blocks.  Bytes: 132 per position of K (128 e4m3 + 4-byte scale) read
     once per launch -- the pool of a prefill chunk, every scored row's own
     positions in decode -- plus the query and weights of scored rows.
     """
     L = wl.seq_len.to(torch.int64).cpu()
     nb = (L + 7) // 8
-    scored = nb > wl.topk_blocks
+    scored = nb > min(wl.topk_blocks, wl.topk + 1)
     positions = int(L[scored].sum())
     flops = 2 * 64 * 128 * positions
     if wl.layout == 1:
@@ -136,7 +136,7 @@ def time_steps(step, steps, warmup, flush, stream, dense_events=True):
         ev[0].record(stream)
         src = wl.layers[0]
         ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, wl.page_table, wl.layout, wl.seq_len,
-                                step.max_len, step.K, step.keys, dev_err=step.dev_err, stream=stream)
+                                step.max_len, step.skip, step.keys, dev_err=step.dev_err, stream=stream)
         ev[1].record(stream)
         step.run_after_dense(stream)
         ev[2].record(stream)
@@ -396,8 +396,8 @@ def main():
 
 
 def head_launches(steps, world):
-    # per step: dense 1 + publish 1 + select 5 (K' == K at the headline workload)
-    return steps * 7
+    # per step: dense 1 + publish 2 (K and P + 1) + select 5
+    return steps * 8
 
 
 if __name__ == "__main__":

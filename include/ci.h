@@ -156,7 +156,7 @@ CI_API int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_l
  *
  * blocks: int32 [rows][blocks_stride]; nvalid: int32 [rows], each
  * 0 <= nvalid[t] <= max_blocks <= min(blocks_stride, 2176).
- * 1 <= topk <= 2048, topk <= out_stride.
+ * 1 <= topk <= 2048, topk <= out_stride; num_pages <= 2^24.
  */
 CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                      int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,

@@ -126,21 +126,21 @@ def check_step(wl, out, rows=None, rep=None):
 
     ``wl``: the CPU workload; ``out``: numpy arrays from the GPU step with keys
     ``keys`` [rows, stride], ``blocks`` / ``nvalid`` (topk_blocks),
-    ``blocks_src`` / ``nvalid_src`` (the source's max(K, P+1) blocks), ``pos``
+    ``blocks_src`` / ``nvalid_src`` (the source's own top P+1 blocks), ``pos``
     [layers, rows, P] and optionally ``score`` [layers, rows, P].
     """
     rep = rep or Report()
     pt = wl.page_table.numpy()
     layout = wl.layout
     K, P = wl.topk_blocks, wl.topk
-    Kp = max(K, P + 1)
+    Kp = P + 1
     rows = range(wl.rows) if rows is None else rows
     seq = wl.seq_len.numpy()
     for t in rows:
         L = int(seq[t])
         nb = O.num_blocks(L)
         logit, tolmag = O.dense_row_scores(wl.layers[0], pt, layout, t, L)
-        if nb > K:
+        if nb > min(K, Kp):
             keys, arg = check_keys(rep, f"row {t} keys", out["keys"][t], L, logit, tolmag)
         else:
             keys, arg = O.block_keys(logit, L)

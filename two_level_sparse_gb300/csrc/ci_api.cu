@@ -136,6 +136,7 @@ int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, 
   if (st != CI_OK) return st;
   if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
   if (max_blocks < 0 || max_blocks > 2176) return CI_ERR_RANGE;
+  if (num_pages > (int64_t{1} << 24)) return CI_ERR_RANGE;  // page ids are packed into 24 bits
   if (rows == 0) return CI_OK;
   if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
   if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;

@@ -10,23 +10,26 @@
 // blocks read from the paged index-K pool, top-512 of the first valid_len
 // columns, page transform to request-relative positions).
 //
-// One persistent CTA per SM works through its rows; every stage is
-// double-buffered so consecutive rows overlap:
+// One persistent CTA per SM works through its rows; consecutive rows overlap:
 //   warp 0      MMA issuer: per row, tcgen05.cp of the row's query scale
 //               factors into tensor memory, then per 128-position tile four
 //               tcgen05.mma kind::mxf8f6f4 block_scale (M = 128 gathered
-//               positions, N = 64 heads, K = 32 each);
-//   warps 1-3   top-k of the previous row from its score buffer (radix select
-//               + ordered compaction), concurrent with the next row's scoring;
-//   warps 4-5   gather: 16-byte cp.async copies of the 16 candidate blocks of
-//               a tile (each block is 1 KB of contiguous K in its page) into
-//               the 128-byte-swizzled MMA tile, plus their fp32 scales; and,
-//               one row ahead, the next row's page lookups, its query widened
-//               from e2m1 to e4m3 and its scale-factor staging;
+//               positions, N = 64 heads, K = 32 each) into one of three
+//               accumulator stages;
+//   warps 1-3   gather: 16-byte cp.async copies of the tile's 16 candidate
+//               blocks (each 1 KB of contiguous K in its page) into a
+//               128-byte-swizzled MMA tile of a 9-deep ring, and their fp32
+//               scales into a separate 16-deep ring; completion is tracked by
+//               the barriers themselves (cp.async.mbarrier.arrive).  Several
+//               warps issue because one warp's copies in flight cap the rate;
+//   warps 4-7   top-k of the previous row, read back from tensor memory, and
+//               then, two rows ahead, the page of every candidate block, the
+//               query widened from e2m1 to e4m3 and its scale factors staged;
 //   warps 8-15  two scoring warpgroups, tiles alternating: the same epilogue
-//               arithmetic as the dense pass, one order-preserving key per
-//               candidate into the row's score buffer in shared memory.
-// Scores never leave the chip.
+//               arithmetic as the dense pass, then one order-preserving key
+//               per candidate stored as one tensor-memory column per tile.
+// Scores never leave the chip, and the shared memory they would need goes to
+// the gather ring instead.
 #include "ci_common.cuh"
 #include "ci_internal.h"
 
@@ -34,25 +37,32 @@ namespace ci {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 3;
-constexpr int kLag = 1;  // cp.async groups a gather thread keeps in flight before signalling
-constexpr int kNumAcc = 6;
-constexpr int kSfaCol = 384;  // 4 columns of A scale factors (all 1.0)
-constexpr int kSfbCol = 392;  // two buffers of 4 columns of B scale factors
+constexpr int kStages = 9;       // gathered K tiles in flight
+constexpr int kScaleSlots = 16;  // scale ring (released by the scoring warps)
+constexpr int kNumAcc = 3;
+constexpr int kSfaCol = 192;      // 4 columns of A scale factors (all 1.0)
+constexpr int kSfbCol = 196;      // two buffers of 4 columns of B scale factors
+constexpr int kScoreCol = 208;    // two buffers of kMaxTiles score columns
 constexpr int kBlocksPerTile = kTileM / kBlock;  // 16
-constexpr int kMaxBlocks = 2176;  // >= topk + 1 for every supported topk
-constexpr int kTopkWarp0 = 1, kTopkThreads = 96, kTopkBar = 2;
-constexpr int kGatherWarp0 = 4, kGatherThreads = 64;
+constexpr int kMaxBlocks = 2176;                 // >= topk + 1 for every supported topk
+constexpr int kMaxTiles = kMaxBlocks / kBlocksPerTile;  // 136
+constexpr int kGatherWarp0 = 1, kGatherWarps = 3;
+constexpr int kTopkWarp0 = 4, kTopkThreads = 128, kTopkBar = 2;  // also the next-row prep
+constexpr int kPrepThreads = kTopkThreads;
 constexpr int kScoreWarp0 = 8;
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;
+static_assert(kScoreCol + 2 * kMaxTiles + 32 <= 512, "score columns must fit in tensor memory");
 
 struct __align__(1024) Smem {
   uint8_t kv[kStages][kTileM * kDim];  // gathered A tiles (1024-aligned)
   uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered
   uint8_t sf[2][512];                  // query scale factors staged for tcgen05.cp
-  float ks[kStages][kTileM];           // K scales of each stage
-  int32_t info[2][kMaxBlocks];         // per candidate: (page << 3) | (block & 7), or -1
+  float ks[kScaleSlots][kTileM];       // K scales
+  // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
+  int32_t info[2][kMaxBlocks];
+  uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
   uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
   uint64_t t_full[kNumAcc], t_empty[kNumAcc];
   uint64_t q_full[2], q_empty[2];
   uint64_t info_full[2], info_empty[2];
@@ -62,8 +72,9 @@ struct __align__(1024) Smem {
   int abort_flag;
   int vcount[2];
   int topk_go;
+  int prep_ok[4];
+  uint32_t kmin, kmax;
   TopkShared topk;
-  // followed by the score keys: 2 x round_up(max_blocks, 16) * 8 uint32
 };
 
 __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
@@ -95,7 +106,7 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int row, bool r
   return r;
 }
 
-// Ring position: stage index and phase parity, advanced one tile at a time.
+// Ring position: slot index and phase parity, advanced one tile at a time.
 struct Ring {
   uint32_t idx = 0, phase = 0;
   __device__ __forceinline__ void next(uint32_t n) {
@@ -106,54 +117,198 @@ struct Ring {
   }
 };
 
-// Gather threads: the next row's query (e2m1 -> e4m3, swizzled), its scale
-// factors staged for tcgen05.cp, and its candidates' page lookups.
-__device__ __forceinline__ void prep_row(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int gt,
+// Prep threads, one row ahead: the query widened from e2m1 to e4m3 into the
+// swizzled B tile, its scale factors staged for tcgen05.cp, and for every
+// candidate block its physical page, its slot in the page and how many of its
+// positions lie below L.
+__device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
                                          volatile int* abort_flag) {
   const int b = ri & 1;
   const uint32_t ph = (ri >> 1) & 1;
-  // the query buffer is free once the MMAs of row ri - 2 completed
-  bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);
-  for (int idx = gt; ok && idx < kHeads * 8; idx += kGatherThreads) {
+  bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
+  for (int idx = pid_t; ok && idx < kHeads * 8; idx += kPrepThreads) {
     const int head = idx >> 3, c = idx & 7;
     const uint2 packed =
         *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(r.row) * kHeads + head) * 64 + c * 8);
     *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(head, c * 16)) = widen_fp4x16(packed);
   }
-  if (ok && gt < 32) {
+  if (ok && pid_t < 32) {
     // lane l of the scale-factor columns: heads l and 32 + l, byte j = K block j
     const uint32_t* sfp = reinterpret_cast<const uint32_t*>(a.p.q_sf + static_cast<int64_t>(r.row) * kHeads * 4);
-    *reinterpret_cast<uint4*>(sm.sf[b] + 16 * gt) = make_uint4(sfp[gt], sfp[32 + gt], kUnitScales, kUnitScales);
+    *reinterpret_cast<uint4*>(sm.sf[b] + 16 * pid_t) =
+        make_uint4(sfp[pid_t], sfp[32 + pid_t], kUnitScales, kUnitScales);
   }
   fence_proxy_async_smem();
   mbar_arrive(&sm.q_full[b]);
-  // page lookups of the candidates, once the previous user of the buffer is done
-  ok = ok && warp_wait(&sm.info_empty[b], ph ^ 1, abort_flag);
+  ok = ok && warp_wait(&sm.info_empty[b], ph ^ 1, abort_flag);  // row ri - 2 gathered and scored
   const int req = a.p.layout == 1 ? 0 : r.row;
   const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
   const int32_t* brow = a.blocks + static_cast<int64_t>(r.row) * a.blocks_stride;
-  for (int i = gt; ok && i < r.nv; i += kGatherThreads) {
-    const int blk = brow[i];
-    int v = -1;
-    if (blk < 0 || blk >= r.nb) {
-      report(a.p.dev_err, kDevErrBlock);
-    } else {
-      const int pid = pt[blk >> 3];
-      if (pid < 0 || pid >= a.p.num_pages)
+  constexpr int kBatch = 16;
+  for (int i0 = 0; ok && i0 < r.nv; i0 += kPrepThreads * kBatch) {
+    int blk[kBatch], pid[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kPrepThreads + pid_t;
+      blk[j] = i < r.nv ? brow[i] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) pid[j] = (blk[j] >= 0 && blk[j] < r.nb) ? pt[blk[j] >> 3] : -1;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kPrepThreads + pid_t;
+      if (i >= r.nv) continue;
+      int v = -1;
+      if (blk[j] < 0 || blk[j] >= r.nb)
+        report(a.p.dev_err, kDevErrBlock);
+      else if (pid[j] < 0 || pid[j] >= a.p.num_pages)
         report(a.p.dev_err, kDevErrPage);
       else
-        v = (pid << 3) | (blk & 7);
+        v = (pid[j] << 7) | ((blk[j] & 7) << 4) | min(kBlock, r.L - blk[j] * kBlock);
+      sm.info[b][i] = v;
     }
-    sm.info[b][i] = v;
   }
   mbar_arrive(&sm.info_full[b]);
+  return ok;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    select_kernel(const SelectArgs a, const int score_cap) {
+// Top-k of one row whose order keys sit in tensor memory: column t of the
+// buffer holds tile t, lane p the tile's position p (key 0 = no candidate).
+// Run by the 128 threads of warps 4-7, thread kt owning lane kt.
+template <class Emit>
+__device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, int k, int kt, Emit emit) {
+  TopkShared& sh = sm.topk;
+  const int q = kt >> 5, l = kt & 31;
+  uint32_t x[32];
+  // live range: the bits below the common prefix of the smallest and largest live key
+  if (kt == 0) {
+    sm.kmin = 0xFFFFFFFFu;
+    sm.kmax = 0;
+  }
+  named_sync(kTopkBar, kTopkThreads);
+  uint32_t mn = 0xFFFFFFFFu, mx = 0;
+  for (int c0 = 0; c0 < nt; c0 += 32) {
+    tmem_ld32(lane_col0 + c0, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c0 + j < nt && x[j] != 0) {
+        mn = min(mn, x[j]);
+        mx = max(mx, x[j]);
+      }
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (l == 0) {
+    atomicMin(&sm.kmin, mn);
+    atomicMax(&sm.kmax, mx);
+  }
+  named_sync(kTopkBar, kTopkThreads);
+  mn = sm.kmin;
+  mx = sm.kmax;
+  int hi = mn == mx ? 0 : 32 - __clz(mn ^ mx);  // low bits not shared by every live key
+  uint32_t mask = hi == 32 ? 0u : ~((1u << hi) - 1u);
+  uint32_t prefix = mn & mask;
+  int remaining = k;
+  while (hi > 0) {
+    const int width = min(8, hi), shift = hi - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int i = kt; i < 256; i += kTopkThreads) sh.hist[i] = 0;
+    named_sync(kTopkBar, kTopkThreads);
+    for (int c0 = 0; c0 < nt; c0 += 32) {
+      tmem_ld32(lane_col0 + c0, x);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < nt && (x[j] & mask) == prefix) atomicAdd(&sh.hist[(x[j] >> shift) & dmask], 1u);
+    }
+    named_sync(kTopkBar, kTopkThreads);
+    if (kt < 32) {
+      uint32_t c[8], lane_sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sh.hist[kt * 8 + j];
+        lane_sum += c[j];
+      }
+      uint32_t suffix = lane_sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, suffix, off);
+        if (kt + off < 32) suffix += v;
+      }
+      const uint32_t above = suffix - lane_sum;
+      if (above < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= suffix) {
+        uint32_t acc = above;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+          if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
+            sh.sel_digit = kt * 8 + j;
+            sh.sel_remaining = remaining - acc;
+            sh.sel_match = c[j];
+            break;
+          }
+          acc += c[j];
+        }
+      }
+    }
+    named_sync(kTopkBar, kTopkThreads);
+    const uint32_t d = sh.sel_digit, match = sh.sel_match;
+    remaining = static_cast<int>(sh.sel_remaining);
+    prefix |= d << shift;
+    mask |= dmask << shift;
+    hi = shift;
+    if (match == static_cast<uint32_t>(remaining)) break;
+  }
+  const uint32_t need_eq = static_cast<uint32_t>(remaining);
+  // ordered compaction: ballots per (tile, warp), then ranks in index order
+  for (int c0 = 0; c0 < nt; c0 += 32) {
+    tmem_ld32(lane_col0 + c0, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (c0 + j >= nt) break;
+      const uint32_t m = x[j] & mask;
+      const uint32_t bg = __ballot_sync(0xffffffffu, m > prefix);
+      const uint32_t be = __ballot_sync(0xffffffffu, m == prefix);
+      if (l == 0) {
+        reinterpret_cast<uint32_t*>(&sm.mgt[c0 + j])[q] = bg;
+        reinterpret_cast<uint32_t*>(&sm.meq[c0 + j])[q] = be;
+      }
+    }
+  }
+  named_sync(kTopkBar, kTopkThreads);
+  const uint32_t lt = lanemask_lt();
+  uint32_t run_gt = 0, run_eq = 0;
+  for (int c0 = 0; c0 < nt; c0 += 32) {
+    tmem_ld32(lane_col0 + c0, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int t = c0 + j;
+      if (t >= nt) break;
+      const uint4 g4 = sm.mgt[t], e4 = sm.meq[t];
+      const uint32_t g[4] = {g4.x, g4.y, g4.z, g4.w}, e[4] = {e4.x, e4.y, e4.z, e4.w};
+      uint32_t gtb = run_gt, eqb = run_eq;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        if (w < q) {
+          gtb += __popc(g[w]);
+          eqb += __popc(e[w]);
+        }
+        run_gt += __popc(g[w]);
+        run_eq += __popc(e[w]);
+      }
+      const bool is_gt = (g[q] >> l) & 1u, is_eq = (e[q] >> l) & 1u;
+      const uint32_t eq_rank = eqb + __popc(e[q] & lt);
+      if (is_gt || (is_eq && eq_rank < need_eq))
+        emit(static_cast<int>(gtb + __popc(g[q] & lt) + min(eq_rank, need_eq)), t, kt, x[j]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint32_t* scores = reinterpret_cast<uint32_t*>(&sm + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -163,18 +318,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], kGatherThreads);
-      mbar_init(&sm.k_empty[s], 1 + 4);
+      mbar_init(&sm.k_full[s], 32 * kGatherWarps);  // one cp.async-tracked arrival per gather lane
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kScaleSlots; ++s) {
+      mbar_init(&sm.s_full[s], 32);
+      mbar_init(&sm.s_empty[s], 4);
     }
     for (int s = 0; s < kNumAcc; ++s) {
       mbar_init(&sm.t_full[s], 1);
       mbar_init(&sm.t_empty[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.q_full[b], kGatherThreads);
+      mbar_init(&sm.q_full[b], kPrepThreads);
       mbar_init(&sm.q_empty[b], 1);
-      mbar_init(&sm.info_full[b], kGatherThreads);
-      mbar_init(&sm.info_empty[b], kGatherThreads);
+      mbar_init(&sm.info_full[b], kPrepThreads);
+      mbar_init(&sm.info_empty[b], 32 * kGatherWarps + 8);  // gather lanes + scoring warps
       mbar_init(&sm.sc_full[b], 8);
       mbar_init(&sm.sc_empty[b], 1);
       sm.vcount[b] = 0;
@@ -187,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
-  if (warp >= kScoreWarp0 && warp < kScoreWarp0 + 4) {
+  if (warp >= kTopkWarp0 && warp < kTopkWarp0 + 4) {
     // A scale factors: all ones, in every lane quadrant
     tmem_st4(tmem_addr(tbase, 32 * (warp & 3), kSfaCol), kUnitScales, kUnitScales, kUnitScales, kUnitScales);
     tmem_st_wait();
@@ -202,11 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       Ring kr, ar;
       int ri = 0;
-      for (int row = blockIdx.x; row < rows; row += gridDim.x, ++ri) {
+      bool ok = true;
+      for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
         const RowInfo r = row_info(a, row, true);
         const int b = ri & 1;
         if (!mbar_wait(&sm.q_full[b], (ri >> 1) & 1, abort_flag)) {
-          set_abort(sm, a.p.dev_err);
+          ok = false;
           break;
         }
         tc_fence_after();
@@ -219,11 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q[b]) + 32 * k);
           idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
         }
-        bool ok = true;
-        for (int t = 0; t < r.ntiles && ok; ++t) {
-          ok = mbar_wait(&sm.k_full[kr.idx], kr.phase, abort_flag) &&
-               mbar_wait(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag);
-          if (!ok) break;
+        for (int t = 0; t < r.ntiles; ++t) {
+          if (!mbar_wait(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
+              !mbar_wait(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
           tc_fence_after();
           const uint32_t d = tbase + ar.idx * kHeads;
           const uint32_t a0 = smem_u32(sm.kv[kr.idx]);
@@ -235,150 +397,117 @@ __global__ void __launch_bounds__(kThreads, 1)
           kr.next(kStages);
           ar.next(kNumAcc);
         }
-        if (!ok) {
-          set_abort(sm, a.p.dev_err);
-          break;
-        }
-        mma_commit(&sm.q_empty[b]);  // the query buffer is free once these MMAs complete
+        if (ok) mma_commit(&sm.q_empty[b]);  // the query buffer is free once these MMAs complete
       }
+      if (!ok) set_abort(sm, a.p.dev_err);
     }
     __syncwarp();
-  } else if (warp >= kTopkWarp0 && warp < kTopkWarp0 + 3) {
-    // ------------------------------------------------------------------ top-k of finished rows
-    const int kt = tid - kTopkWarp0 * 32;
-    int ri = 0;
-    for (int row = blockIdx.x; row < rows; row += gridDim.x, ++ri) {
-      const RowInfo r = row_info(a, row, false);
-      const int b = ri & 1;
-      if (kt == 0) sm.topk_go = mbar_wait(&sm.sc_full[b], (ri >> 1) & 1, abort_flag) ? 1 : 0;
-      named_sync(kTopkBar, kTopkThreads);
-      const int go = sm.topk_go;
-      if (!go) {
-        if (kt == 0) set_abort(sm, a.p.dev_err);
-        break;
-      }
-      // every scoring warp arrived on sc_full after its stores; the barrier
-      // above gives the other top-k threads the same view
-      const int k = min(a.topk, sm.vcount[b]);
-      const int32_t* brow = a.blocks + static_cast<int64_t>(row) * a.blocks_stride;
-      int32_t* out = a.out_pos + static_cast<int64_t>(row) * a.out_stride;
-      float* osc = a.out_score != nullptr ? a.out_score + static_cast<int64_t>(row) * a.out_stride : nullptr;
-      const uint32_t* sc = scores + b * score_cap;
-      if (k > 0) {
-        block_topk(sc, r.nv * kBlock, k, sm.topk, kt, kTopkThreads, kTopkBar, [&](int rank, int idx, uint32_t u) {
-          out[rank] = brow[idx >> 3] * kBlock + (idx & 7);
-          if (osc) osc[rank] = order_key_inv(u);
-        });
-      }
-      for (int i = max(k, 0) + kt; i < a.topk; i += kTopkThreads) {
-        out[i] = -1;
-        if (osc) osc[i] = -__int_as_float(0x7f800000);
-      }
-      named_sync(kTopkBar, kTopkThreads);
-      if (kt == 0) {
-        sm.vcount[b] = 0;
-        mbar_arrive(&sm.sc_empty[b]);
-      }
-    }
-  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 2) {
-    // ------------------------------------------------------------------ gather + next-row prep
-    const int gt = tid - kGatherWarp0 * 32;  // 0..63
-    const int g = gt >> 5;                   // this warp's half of each tile: blocks 8g .. 8g+7
-    Ring kr;
-    uint32_t issued = 0, signalled = 0;
+  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
+    // ------------------------------------------------------------------ gather
+    const int gw = warp - kGatherWarp0;
+    Ring kr, sr;
     int ri = 0;
     bool ok = true;
-    int row = blockIdx.x;
-    RowInfo r{};
-    if (row < rows) {
-      r = row_info(a, row, false);
-      prep_row(sm, a, r, 0, gt, abort_flag);
-    }
-    for (; row < rows && ok; row += gridDim.x, ++ri) {
+    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
+      const RowInfo r = row_info(a, row, false);
       const int b = ri & 1;
-      const int next_row = row + gridDim.x;
-      const RowInfo rn = next_row < rows ? row_info(a, next_row, false) : RowInfo{};
-      const int prep_at = min(kStages, r.ntiles);
-      const uint32_t row_start = issued;
-      bool prepped = next_row >= rows;
-      // the next row's prep waits for the MMAs of the previous row: every one of
-      // its tiles must have been signalled first
-      auto flush_previous = [&]() {
-        if (signalled < row_start) {
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          while (signalled < issued) {
-            mbar_arrive(&sm.k_full[signalled % kStages]);
-            ++signalled;
-          }
-        }
-      };
       ok = warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t) {
-        if (t == prep_at && !prepped) {
-          flush_previous();
-          prep_row(sm, a, rn, ri + 1, gt, abort_flag);
-          prepped = true;
-        }
-        if (!warp_wait(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
+        if ((gw == 0 && !warp_wait(&sm.s_empty[sr.idx], sr.phase ^ 1, abort_flag)) ||
+            !warp_wait(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
+        if (gw == 0) {  // scales: lane l copies half of block l / 2's eight fp32 scales
+          const int blk = lane >> 1, half = lane & 1;
+          const int slot = t * kBlocksPerTile + blk;
+          const int v = slot < r.nv ? info[slot] : -1;
+          if (v >= 0)
+            cp_async16(&sm.ks[sr.idx][blk * kBlock + half * 4],
+                       a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + kPageValueBytes +
+                           (((v >> 4) & 7) * kBlock + half * 4) * 4);
+          cp_async_arrive_noinc(&sm.s_full[sr.idx]);
+        }
         uint8_t* dst = sm.kv[kr.idx];
 #pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
-          const int blk = 8 * g + (j >> 1);
+        for (int j = gw; j < 32; j += kGatherWarps) {
+          const int blk = j >> 1;  // instruction j: 512 contiguous bytes of block j / 2
           const int slot = t * kBlocksPerTile + blk;
           const int v = slot < r.nv ? info[slot] : -1;
           if (v >= 0) {
             const int o = (j & 1) * 32 + lane;  // 16-byte chunk of the block's 1 KB
             const uint8_t* src =
-                a.p.k_pool + static_cast<int64_t>(v >> 3) * kPageBytes + (v & 7) * (kBlock * kDim) + o * 16;
+                a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + ((v >> 4) & 7) * (kBlock * kDim) + o * 16;
             cp_async16(dst + sw128_offset(blk * kBlock + (o >> 3), (o & 7) * 16), src);
           }
         }
-        if (lane < 16) {
-          const int blk = 8 * g + (lane >> 1), half = lane & 1;
-          const int slot = t * kBlocksPerTile + blk;
-          const int v = slot < r.nv ? info[slot] : -1;
-          if (v >= 0)
-            cp_async16(&sm.ks[kr.idx][blk * kBlock + half * 4],
-                       a.p.k_pool + static_cast<int64_t>(v >> 3) * kPageBytes + kPageValueBytes +
-                           ((v & 7) * kBlock + half * 4) * 4);
-        }
-        cp_async_commit();
-        ++issued;
-        if (issued - signalled > kLag) {
-          cp_async_wait<kLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(&sm.k_full[signalled % kStages]);
-          ++signalled;
-        }
+        cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         kr.next(kStages);
+        sr.next(kScaleSlots);
       }
-      if (!ok) break;
-      if (!prepped) {
-        flush_previous();
-        prep_row(sm, a, rn, ri + 1, gt, abort_flag);
-        prepped = true;
-      }
-      mbar_arrive(&sm.info_empty[b]);
-      r = rn;
+      __syncwarp();
+      if (ok) mbar_arrive(&sm.info_empty[b]);
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    while (signalled < issued) {
-      mbar_arrive(&sm.k_full[signalled % kStages]);
-      ++signalled;
-    }
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
+  } else if (warp >= kTopkWarp0 && warp < kTopkWarp0 + 4) {
+    // ------------------------------------------------------------------ top-k of finished rows + next-row prep
+    const int kt = tid - kTopkWarp0 * 32;
+    const uint32_t lane_base = tmem_addr(tbase, 32 * (warp & 3), 0);
+    // prep of row index pi (the pi-th row of this CTA); the verdict is made uniform
+    // across the four warps before anyone acts on it
+    auto prep = [&](int pi) -> bool {
+      const int prow = blockIdx.x + pi * gridDim.x;
+      const bool mine = prow >= rows || prep_row(sm, a, row_info(a, prow, false), pi, kt, abort_flag);
+      if (lane == 0) sm.prep_ok[warp & 3] = mine ? 1 : 0;
+      named_sync(kTopkBar, kTopkThreads);
+      const bool all = sm.prep_ok[0] && sm.prep_ok[1] && sm.prep_ok[2] && sm.prep_ok[3];
+      named_sync(kTopkBar, kTopkThreads);
+      return all;
+    };
+    bool ok = prep(0) && prep(1);
+    int ri = 0;
+    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
+      const RowInfo r = row_info(a, row, false);
+      const int b = ri & 1;
+      if (kt == 0) sm.topk_go = mbar_wait(&sm.sc_full[b], (ri >> 1) & 1, abort_flag) ? 1 : 0;
+      named_sync(kTopkBar, kTopkThreads);
+      if (!sm.topk_go) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k = min(a.topk, sm.vcount[b]);
+      const int32_t* brow = a.blocks + static_cast<int64_t>(row) * a.blocks_stride;
+      int32_t* out = a.out_pos + static_cast<int64_t>(row) * a.out_stride;
+      float* osc = a.out_score != nullptr ? a.out_score + static_cast<int64_t>(row) * a.out_stride : nullptr;
+      if (k > 0) {
+        tmem_topk(sm, lane_base + kScoreCol + b * kMaxTiles, r.ntiles, k, kt,
+                  [&](int rank, int t, int p, uint32_t u) {
+                    out[rank] = brow[t * kBlocksPerTile + (p >> 3)] * kBlock + (p & 7);
+                    if (osc) osc[rank] = order_key_inv(u);
+                  });
+      }
+      for (int i = max(k, 0) + kt; i < a.topk; i += kTopkThreads) {
+        out[i] = -1;
+        if (osc) osc[i] = -__int_as_float(0x7f800000);
+      }
+      tc_fence_before();
+      named_sync(kTopkBar, kTopkThreads);
+      if (kt == 0) {
+        sm.vcount[b] = 0;
+        mbar_arrive(&sm.sc_empty[b]);
+      }
+      ok = prep(ri + 2);
+    }
+    if (!ok && kt == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kScoreWarp0) {
     // ------------------------------------------------------------------ scoring epilogue
     const int e = (warp - kScoreWarp0) >> 2;  // scoring warpgroup 0 / 1
     const int quad = warp & 3;
     const int p = 32 * quad + lane;
-    Ring kr, ar;
+    Ring sr, ar;
     uint32_t tseq = 0;
     int ri = 0;
     float w[kHeads];
@@ -386,7 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
       const RowInfo r = row_info(a, row, false);
       const int b = ri & 1;
-      uint32_t* sc = scores + b * score_cap;
       const float4* wp = reinterpret_cast<const float4*>(a.p.w + static_cast<int64_t>(row) * kHeads);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -396,16 +524,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         w[4 * j + 2] = v.z;
         w[4 * j + 3] = v.w;
       }
-      const int32_t* brow = a.blocks + static_cast<int64_t>(row) * a.blocks_stride;
-      // the score buffer must have been read by the top-k of row ri - 2
-      if (ri >= 2 && !warp_wait(&sm.sc_empty[b], ((ri >> 1) & 1) ^ 1, abort_flag)) {
+      // the candidate page lookups (prepared with the row) tell which positions are live
+      if (!warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag) ||
+          (ri >= 2 && !warp_wait(&sm.sc_empty[b], ((ri >> 1) & 1) ^ 1, abort_flag))) {
         ok = false;
         break;
       }
+      tc_fence_after();
+      const uint32_t score_col = tmem_addr(tbase, 32 * quad, kScoreCol + b * kMaxTiles);
       uint32_t nvalid_seen = 0;
       for (int t = 0; t < r.ntiles; ++t, ++tseq) {
-        const bool mine = (tseq & 1) == static_cast<uint32_t>(e);
-        if (mine) {
+        if ((tseq & 1) == static_cast<uint32_t>(e)) {
+          const int slot = t * kBlocksPerTile + (p >> 3);
+          const int v = slot < r.nv ? sm.info[b][slot] : -1;
+          const bool valid = v >= 0 && (p & 7) < (v & 15);
           if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
             ok = false;
             break;
@@ -424,29 +556,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.t_empty[ar.idx]);
           const float score = head_reduce_finish(acc);
-          if (!warp_wait(&sm.k_full[kr.idx], kr.phase, abort_flag)) {
+          if (!warp_wait(&sm.s_full[sr.idx], sr.phase, abort_flag)) {
             ok = false;
             break;
           }
-          const float kscale = sm.ks[kr.idx][p];
+          const float kscale = sm.ks[sr.idx][p];
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.k_empty[kr.idx]);
-          const int slot = t * kBlocksPerTile + (p >> 3);
-          bool valid = false;
-          if (slot < r.nv) {
-            const int blk = brow[slot];
-            valid = blk >= 0 && blk < r.nb && blk * kBlock + (p & 7) < r.L;
-          }
-          sc[t * kTileM + p] = valid ? order_key(score * kscale) : 0u;
+          if (lane == 0) mbar_arrive(&sm.s_empty[sr.idx]);
+          tmem_st1(score_col + t, valid ? order_key(score * kscale) : 0u);
           nvalid_seen += __popc(__ballot_sync(0xffffffffu, valid));
         }
-        kr.next(kStages);
+        sr.next(kScaleSlots);
         ar.next(kNumAcc);
       }
       if (!ok) break;
+      tmem_st_wait();
+      tc_fence_before();
       if (lane == 0 && nvalid_seen) atomicAdd(&sm.vcount[b], static_cast<int>(nvalid_seen));
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.sc_full[b]);
+      if (lane == 0) {
+        mbar_arrive(&sm.sc_full[b]);
+        mbar_arrive(&sm.info_empty[b]);  // done reading this row's candidate lookups
+      }
     }
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
   }
@@ -466,19 +597,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t select_smem_bytes(int max_blocks) {
-  const size_t cap = static_cast<size_t>((max_blocks + kBlocksPerTile - 1) / kBlocksPerTile) * kTileM;
-  return sizeof(Smem) + 2 * cap * 4 + 1024;
-}
+size_t select_smem_bytes(int) { return sizeof(Smem) + 1024; }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   if (a.p.rows == 0) return cudaSuccess;
-  const int cap = ((a.max_blocks + kBlocksPerTile - 1) / kBlocksPerTile) * kTileM;
   const int smem = static_cast<int>(select_smem_bytes(a.max_blocks));
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = min(device_sm_count(), a.p.rows);
-  select_kernel<<<grid, kThreads, smem, stream>>>(a, cap);
+  select_kernel<<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

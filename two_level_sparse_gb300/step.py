@@ -5,16 +5,16 @@ Call sequence (sglang PR #40352, Design: the source computes its dense scores,
 publishes its candidate blocks and runs its own top-512; each consumer selects
 within the published blocks):
 
-  ci_score_dense_amax8(source)                   keys, rows with > K blocks
-  ci_publish_blocks(keys, K')                    the source's own candidates
-  ci_publish_blocks(keys, K)        (if K' != K) the consumers' candidates
-  ci_select_sparse(source, K' blocks)            the source's top-P
+  ci_score_dense_amax8(source)                   keys, rows with > min(K, P+1) blocks
+  ci_publish_blocks(keys, K)                     the consumers' candidates
+  ci_publish_blocks(keys, P + 1)  (if P+1 != K)  the source's own candidates
+  ci_select_sparse(source, P + 1 blocks)         the source's top-P
   ci_select_sparse(consumer j, K blocks)         each consumer's top-P
 
-with K' = max(K, P + 1): every position of the dense top-P lies in the top
-P + 1 blocks by key (the newest block's key is +inf and every other block that
-outranks a position's block holds a distinct higher-scoring position), so the
-source's top-P over its top-K' blocks is its dense top-P.
+Every position of the dense top-P lies in the top P + 1 blocks by key (the
+newest block's key is +inf and every other block that outranks a position's
+block holds a distinct higher-scoring position), so the source's top-P over
+its top-(P+1) blocks is its dense top-P, and the source gathers only those.
 
 This module only allocates the output buffers (torch device memory) and
 marshals arguments; all computation runs in libci.so.
@@ -34,18 +34,19 @@ class IndexerStep:
         self.max_len = wl.max_len
         self.K = wl.topk_blocks
         self.P = wl.topk
-        self.Kp = max(self.K, self.P + 1)
+        self.Kp = self.P + 1  # the source's own candidate blocks
+        self.skip = min(self.K, self.Kp)  # rows with at most this many blocks need no keys
         nb_max = (self.max_len + 7) // 8
         stride = max(8, (nb_max + 7) // 8 * 8)
         i32 = torch.int32
         self.keys = torch.empty(self.rows, stride, dtype=torch.float32, device=dev)
-        self.blocks_src = torch.empty(self.rows, self.Kp, dtype=i32, device=dev)
-        self.nvalid_src = torch.empty(self.rows, dtype=i32, device=dev)
+        self.blocks = torch.empty(self.rows, self.K, dtype=i32, device=dev)
+        self.nvalid = torch.empty(self.rows, dtype=i32, device=dev)
         if self.Kp == self.K:
-            self.blocks, self.nvalid = self.blocks_src, self.nvalid_src
+            self.blocks_src, self.nvalid_src = self.blocks, self.nvalid
         else:
-            self.blocks = torch.empty(self.rows, self.K, dtype=i32, device=dev)
-            self.nvalid = torch.empty(self.rows, dtype=i32, device=dev)
+            self.blocks_src = torch.empty(self.rows, self.Kp, dtype=i32, device=dev)
+            self.nvalid_src = torch.empty(self.rows, dtype=i32, device=dev)
         nl = len(wl.layers)
         self.pos = torch.empty(nl, self.rows, self.P, dtype=i32, device=dev)
         self.score = torch.empty(nl, self.rows, self.P, dtype=torch.float32, device=dev) if with_scores else None
@@ -64,12 +65,12 @@ class IndexerStep:
         common = dict(page_table=wl.page_table, layout=wl.layout, seq_len=wl.seq_len, max_len=self.max_len,
                       dev_err=self.dev_err, stream=stream)
         if not skip_dense:
-            ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, skip_le_blocks=self.K, keys=self.keys,
+            ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, skip_le_blocks=self.skip, keys=self.keys,
                                     **common)
-        ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.Kp, self.blocks_src, self.nvalid_src,
+        ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
                              dev_err=self.dev_err, stream=stream)
         if self.Kp != self.K:
-            ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
+            ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.Kp, self.blocks_src, self.nvalid_src,
                                  dev_err=self.dev_err, stream=stream)
         for j, layer in enumerate(wl.layers):
             blocks, nvalid, mb = (self.blocks_src, self.nvalid_src, self.Kp) if j == 0 else (self.blocks,
