@@ -11,20 +11,22 @@
 //
 // Design (one persistent CTA per SM, 16 warps):
 //   warp 0      TMA producer: two 64-position pages of FP8 K per 128-position
-//               tile (one tensor-map load each, 128-byte swizzle) plus their
-//               fp32 scales (bulk copy), into an 8-stage ring;
+//               tile (one tensor-map load each, 128-byte swizzle) into an
+//               8-stage ring, their fp32 scales (bulk copies) into a separate
+//               16-slot ring;
 //   warp 1      MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale, M = 128
-//               positions, N = 64 * R columns (R rows x 64 heads), K = 128 in
-//               four K=32 steps; A = K tile (scale 1), B = the rows' queries
+//               positions, N = 64 R columns (R rows x 64 heads), K = 128 in
+//               four K = 32 steps; A = K tile (scale 1), B = the rows' queries
 //               widened from e2m1 to e4m3 (exact) with their ue8m0 scales in
 //               tensor memory; fp32 accumulators in tensor memory;
 //   warps 4-15  epilogue, three warpgroups: tcgen05.ld of one row's 64 head
-//               columns per position, ReLU + head weights (packed fp32x2 FMA),
-//               K scale, length mask, max over 8 lanes, key store.
+//               columns per position, ReLU + head weights, K scale, length
+//               mask, max over 8 lanes by shuffles, key store.
 // Prefill rows share one request's pages, so R = 3 rows ride one MMA
-// (N = 192); decode rows each have their own pages, R = 1 (N = 64) and the
-// three epilogue warpgroups take tiles round-robin.  Work is the list of
-// (row group, 128-position tile) pairs, split evenly across the CTAs.
+// (N = 192, two accumulator stages); decode rows each have their own pages,
+// R = 1 (N = 64, six stages) and the three epilogue warpgroups take tiles
+// round-robin.  Work is the list of (row group, 128-position tile) pairs,
+// split evenly across the CTAs.
 #include "ci_common.cuh"
 #include "ci_internal.h"
 
@@ -33,18 +35,19 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kStages = 8;
+constexpr int kScaleSlots = 16;
 constexpr int kEpiWarp0 = 4;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 384;  // accumulator columns (2 x 192 or 6 x 64)
-constexpr int kSfaCol = 384;   // 4 columns: A scale factors (all 1.0)
-constexpr int kSfbCol = 388;   // 8 columns: B scale factors
+constexpr int kSfaCol = 384;  // 4 columns: A scale factors (all 1.0)
+constexpr int kSfbCol = 388;  // 8 columns: B scale factors
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;
 
 struct __align__(1024) Smem {
   uint8_t kv[kStages][kTileM * kDim];  // A tiles, 1024-aligned
   uint8_t q[3 * kHeads * kDim];        // B tile (up to 192 rows of 128 B)
-  float ks[kStages][kTileM];           // per-position K scales of each stage
+  float ks[kScaleSlots][kTileM];       // per-position K scales
   uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
   uint64_t t_full[6], t_empty[6];
   uint64_t drain;
   uint32_t tmem_base;
@@ -54,21 +57,16 @@ struct __align__(1024) Smem {
   long long warp_sum[kThreads / 32];
 };
 
-struct Geometry {
-  int R;       // rows per group
-  int N;       // MMA N = 64 R
-  int n_acc;   // accumulator stages
-  int epi_per_tile;  // epilogue warpgroups consuming each tile
+// Ring position: slot index and phase parity, advanced one tile at a time.
+struct Ring {
+  uint32_t idx = 0, phase = 0;
+  __device__ __forceinline__ void next(uint32_t n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1;
+    }
+  }
 };
-
-__device__ __forceinline__ Geometry geometry(int layout) {
-  Geometry g;
-  g.R = layout == 1 ? 3 : 1;
-  g.N = 64 * g.R;
-  g.n_acc = kAccCols / g.N;
-  g.epi_per_tile = g.R == 3 ? 3 : 1;
-  return g;
-}
 
 // Length that row `row` is scored over: L if it has more than skip_le_blocks
 // blocks, 0 if skipped, -1 if its length breaks the contract.
@@ -78,14 +76,15 @@ __device__ __forceinline__ int scored_len(const DenseArgs& a, int row) {
   return ((L + kBlock - 1) / kBlock) > a.skip_le_blocks ? L : 0;
 }
 
-__device__ __forceinline__ int group_len(const DenseArgs& a, int g, int R) {
+template <int R>
+__device__ __forceinline__ int group_len(const DenseArgs& a, int g) {
   int m = 0;
-  for (int r = g * R; r < min(a.p.rows, g * R + R); ++r) m = max(m, scored_len(a, r));
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int r = g * R + i;
+    if (r < a.p.rows) m = max(m, scored_len(a, r));
+  }
   return m;
-}
-
-__device__ __forceinline__ int group_tiles(const DenseArgs& a, int g, int R) {
-  return (group_len(a, g, R) + kTileM - 1) / kTileM;
 }
 
 __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
@@ -93,13 +92,16 @@ __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
   report(dev_err, kDevErrTimeout);
 }
 
+template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_amax8_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
+  constexpr int N = 64 * R;                    // MMA N
+  constexpr int kNumAcc = 384 / N;             // accumulator stages
+  constexpr int kEpiPerTile = R == 3 ? 3 : 1;  // epilogue warpgroups consuming each tile
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const Geometry geo = geometry(a.p.layout);
-  const int num_groups = (a.p.rows + geo.R - 1) / geo.R;
+  const int num_groups = (a.p.rows + R - 1) / R;
   volatile int* abort_flag = &sm.abort_flag;
 
   // ---------------------------------------------------------------- set-up
@@ -110,11 +112,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1 + 4 * geo.epi_per_tile);
+      mbar_init(&sm.k_empty[s], 1);
     }
-    for (int s = 0; s < 6; ++s) {
+    for (int s = 0; s < kScaleSlots; ++s) {
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.s_empty[s], 4 * kEpiPerTile);
+    }
+    for (int s = 0; s < kNumAcc; ++s) {
       mbar_init(&sm.t_full[s], 1);
-      mbar_init(&sm.t_empty[s], 4 * geo.epi_per_tile);
+      mbar_init(&sm.t_empty[s], 4 * kEpiPerTile);
     }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -130,9 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g0 = min(num_groups, tid * per), g1 = min(num_groups, g0 + per);
     long long mine = 0;
     for (int g = g0; g < g1; ++g) {
-      for (int r = g * geo.R; r < min(a.p.rows, g * geo.R + geo.R); ++r)
-        if (scored_len(a, r) < 0 && blockIdx.x == 0) report(a.p.dev_err, kDevErrLen);
-      mine += group_tiles(a, g, geo.R);
+      if (blockIdx.x == 0)
+        for (int r = g * R; r < min(a.p.rows, g * R + R); ++r)
+          if (scored_len(a, r) < 0) report(a.p.dev_err, kDevErrLen);
+      mine += (group_len<R>(a, g) + kTileM - 1) / kTileM;
     }
     long long incl = mine;
 #pragma unroll
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tb < te && excl <= tb && tb < excl + mine) {
       long long acc = excl;
       for (int g = g0; g < g1; ++g) {
-        const int n = group_tiles(a, g, geo.R);
+        const int n = (group_len<R>(a, g) + kTileM - 1) / kTileM;
         if (tb < acc + n) {
           sm.g_begin = g;
           sm.o_begin = static_cast<int>(tb - acc);
@@ -181,14 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = sm.tmem_base;
   long long remaining = sm.t_end - sm.t_begin;
   int g = sm.g_begin, off = sm.o_begin;
-  uint32_t kcount = 0, acount = 0;  // tiles issued so far through the rings (same on every role)
-  uint32_t issued = 0;              // TMA thread: tiles whose loads were issued
+  Ring kr, sr, ar;      // same tile sequence on every role
+  uint32_t tseq = 0;    // tiles so far (decode: picks the epilogue warpgroup)
+  uint32_t issued = 0;  // TMA thread: tiles whose loads were issued
   const int epi = warp >= kEpiWarp0 ? (warp - kEpiWarp0) >> 2 : -1;  // epilogue warpgroup
   const int quad = warp & 3;
   float w[kHeads];
 
   while (remaining > 0 && g < num_groups) {
-    const int glen = group_len(a, g, geo.R);
+    const int glen = group_len<R>(a, g);
     const int ntiles = (glen + kTileM - 1) / kTileM;
     const int take = static_cast<int>(min(static_cast<long long>(ntiles - off), remaining));
     if (take <= 0) {
@@ -199,12 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // the previous group is fully consumed
     if (*abort_flag) break;
     // ---- group set-up: queries widened to e4m3 in the swizzled B tile
-    for (int idx = tid; idx < geo.N * 8; idx += kThreads) {
+    for (int idx = tid; idx < N * 8; idx += kThreads) {
       const int n = idx >> 3, c = idx & 7;
-      const int row = g * geo.R + n / kHeads, head = n % kHeads;
+      const int row = g * R + n / kHeads, head = n % kHeads;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (row < a.p.rows) {
-        const uint2 packed = *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(row) * kHeads + head) * 64 + c * 8);
+        const uint2 packed =
+            *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(row) * kHeads + head) * 64 + c * 8);
         v = widen_fp4x16(packed);
       }
       *reinterpret_cast<uint4*>(sm.q + sw128_offset(n, c * 16)) = v;
@@ -216,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int n = 32 * c + lane;
-        const int row = g * geo.R + n / kHeads, head = n % kHeads;
-        sf[c] = (n < geo.N && row < a.p.rows)
+        const int row = g * R + n / kHeads, head = n % kHeads;
+        sf[c] = (n < N && row < a.p.rows)
                     ? *reinterpret_cast<const uint32_t*>(a.p.q_sf + (static_cast<int64_t>(row) * kHeads + head) * 4)
                     : kUnitScales;
       }
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: this warpgroup's row and its head weights
     int row = -1, rlen = 0;
     if (epi >= 0) {
-      row = geo.R == 3 ? g * 3 + epi : g;
+      row = R == 3 ? g * 3 + epi : g;
       if (row < a.p.rows) {
         rlen = max(scored_len(a, row), 0);
         const float4* wp = reinterpret_cast<const float4*>(a.p.w + static_cast<int64_t>(row) * kHeads);
@@ -251,33 +260,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const int req = a.p.layout == 1 ? 0 : g;
         const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
+        Ring k = kr, s = sr;
         for (int t = off; t < off + take; ++t) {
-          const uint32_t i = kcount + (t - off), s = i % kStages, ph = (i / kStages) & 1;
-          if (!mbar_wait(&sm.k_empty[s], ph ^ 1, abort_flag)) {
+          if (!mbar_wait(&sm.k_empty[k.idx], k.phase ^ 1, abort_flag) ||
+              !mbar_wait(&sm.s_empty[s.idx], s.phase ^ 1, abort_flag)) {
             set_abort(sm, a.p.dev_err);
             break;
           }
           const int npos = min(kTileM, glen - t * kTileM);
           const int npages = (npos + kPage - 1) / kPage;
           int pid[2] = {-1, -1};
-          uint32_t bytes = 0;
+          uint32_t nvalid = 0;
           for (int j = 0; j < npages; ++j) {
             const int p = pt[t * 2 + j];
             if (p < 0 || p >= a.p.num_pages) {
               report(a.p.dev_err, kDevErrPage);
             } else {
               pid[j] = p;
-              bytes += kPageValueBytes + kPage * 4;
+              ++nvalid;
             }
           }
-          mbar_arrive_expect_tx(&sm.k_full[s], bytes);
+          mbar_arrive_expect_tx(&sm.k_full[k.idx], nvalid * kPageValueBytes);
+          mbar_arrive_expect_tx(&sm.s_full[s.idx], nvalid * kPage * 4);
           for (int j = 0; j < npages; ++j) {
             if (pid[j] < 0) continue;
-            tma_load_3d(sm.kv[s] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[s]);
-            bulk_load(&sm.ks[s][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes,
-                      kPage * 4, &sm.k_full[s]);
+            tma_load_3d(sm.kv[k.idx] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[k.idx]);
+            bulk_load(&sm.ks[s.idx][j * kPage],
+                      a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, kPage * 4,
+                      &sm.s_full[s.idx]);
           }
           ++issued;
+          k.next(kStages);
+          s.next(kScaleSlots);
         }
       }
       __syncwarp();
@@ -289,23 +303,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q) + 32 * k);
-          idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, geo.N, k, k);
+          idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, N, k, k);
         }
+        Ring k = kr, acc = ar;
         for (int t = off; t < off + take; ++t) {
-          const uint32_t i = kcount + (t - off), s = i % kStages, ph = (i / kStages) & 1;
-          const uint32_t ai = acount + (t - off), acc = ai % geo.n_acc, aph = (ai / geo.n_acc) & 1;
-          if (!mbar_wait(&sm.k_full[s], ph, abort_flag) || !mbar_wait(&sm.t_empty[acc], aph ^ 1, abort_flag)) {
+          if (!mbar_wait(&sm.k_full[k.idx], k.phase, abort_flag) ||
+              !mbar_wait(&sm.t_empty[acc.idx], acc.phase ^ 1, abort_flag)) {
             set_abort(sm, a.p.dev_err);
             break;
           }
           tc_fence_after();
-          const uint32_t d = tbase + acc * geo.N;
-          const uint32_t a0 = smem_u32(sm.kv[s]);
+          const uint32_t d = tbase + acc.idx * N;
+          const uint32_t a0 = smem_u32(sm.kv[k.idx]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_mxf8f6f4(d, sdesc_k128_sw128(a0 + 32 * k), bdesc[k], idesc[k], tbase + kSfaCol, tbase + kSfbCol, k);
-          mma_commit(&sm.k_empty[s]);
-          mma_commit(&sm.t_full[acc]);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf8f6f4(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol, tbase + kSfbCol,
+                         kk);
+          mma_commit(&sm.k_empty[k.idx]);
+          mma_commit(&sm.t_full[acc.idx]);
+          k.next(kStages);
+          acc.next(kNumAcc);
         }
       }
       __syncwarp();
@@ -314,20 +331,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int p = 32 * quad + lane;
       const int nb = (rlen + kBlock - 1) / kBlock;
       float* keys_row = row >= 0 && row < a.p.rows ? a.keys + static_cast<int64_t>(row) * a.keys_stride : nullptr;
-      const uint32_t col0 = geo.R == 3 ? epi * kHeads : 0;
-      for (int t = off; t < off + take; ++t) {
-        const uint32_t ai = acount + (t - off);
-        if (geo.R == 1 && static_cast<int>(ai % 3) != epi) continue;
-        const uint32_t acc = ai % geo.n_acc, aph = (ai / geo.n_acc) & 1;
-        const uint32_t i = kcount + (t - off), s = i % kStages, ph = (i / kStages) & 1;
-        if (!warp_wait(&sm.t_full[acc], aph, abort_flag)) {
+      const uint32_t col0 = R == 3 ? epi * kHeads : 0;
+      Ring s = sr, acc = ar;
+      uint32_t ts = tseq;
+      for (int t = off; t < off + take; ++t, ++ts, s.next(kScaleSlots), acc.next(kNumAcc)) {
+        if (R == 1 && static_cast<int>(ts % 3) != epi) continue;
+        if (!warp_wait(&sm.t_full[acc.idx], acc.phase, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           break;
         }
         tc_fence_after();
         float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint32_t x[32];
-        const uint32_t taddr = tmem_addr(tbase, 32 * quad, acc * geo.N + col0);
+        const uint32_t taddr = tmem_addr(tbase, 32 * quad, acc.idx * N + col0);
         tmem_ld32(taddr, x);
         tmem_ld_wait();
         head_reduce_half(part, x, w);
@@ -336,15 +352,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         head_reduce_half(part, x, w + 32);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.t_empty[acc]);
+        if (lane == 0) mbar_arrive(&sm.t_empty[acc.idx]);
         const float score = head_reduce_finish(part);
-        if (!warp_wait(&sm.k_full[s], ph, abort_flag)) {
+        if (!warp_wait(&sm.s_full[s.idx], s.phase, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           break;
         }
-        const float kscale = sm.ks[s][p];
+        const float kscale = sm.ks[s.idx][p];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.k_empty[s]);
+        if (lane == 0) mbar_arrive(&sm.s_empty[s.idx]);
         const int pos = t * kTileM + p;
         const bool valid = keys_row != nullptr && pos < rlen;
         float v = valid ? score * kscale : -__int_as_float(0x7f800000);
@@ -357,8 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    kcount += take;
-    acount += take;
+    for (int i = 0; i < take; ++i) {
+      kr.next(kStages);
+      sr.next(kScaleSlots);
+      ar.next(kNumAcc);
+    }
+    tseq += take;
     remaining -= take;
     ++g;
     off = 0;
@@ -373,8 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm.drain, 0, nullptr, 1000000000ull);
     }
     if (warp == 0 && lane == 0) {
-      for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+      for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
         mbar_wait(&sm.k_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
+        mbar_wait(&sm.s_full[i % kScaleSlots], (i / kScaleSlots) & 1, nullptr, 1000000000ull);
+      }
     }
   }
   tc_fence_before();
@@ -389,9 +411,15 @@ cudaError_t launch_dense_amax8(const DenseArgs& a, cudaStream_t stream) {
   cudaError_t e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, kPage);
   if (e != cudaSuccess) return e;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
-  e = cudaFuncSetAttribute(dense_amax8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dense_amax8_kernel<<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
+  if (a.p.layout == 1) {
+    e = cudaFuncSetAttribute(dense_amax8_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dense_amax8_kernel<3><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
+  } else {
+    e = cudaFuncSetAttribute(dense_amax8_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dense_amax8_kernel<1><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
+  }
   return cudaGetLastError();
 }
 
