@@ -61,6 +61,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+// The common case first: every lane probes once and the warp votes; only when
+// the phase is not complete yet does it fall back to the bounded wait.
+__device__ __forceinline__ bool warp_wait_fast(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return warp_wait(bar, parity, abort);
+}
+
 // ---------------------------------------------------------------- score epilogue
 // Head-weighted ReLU reduction of one (row, position) pair from its 64 fp32
 // accumulator columns, delivered in two halves of 32: eight partial sums

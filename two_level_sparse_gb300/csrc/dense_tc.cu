@@ -34,8 +34,8 @@ namespace ci {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 8;
-constexpr int kScaleSlots = 16;
+constexpr int kStages = 8;       // K ring (power of two: slot and phase come from the tile counter)
+constexpr int kScaleSlots = 16;  // scale ring (power of two)
 constexpr int kEpiWarp0 = 4;
 constexpr int kTmemCols = 512;
 constexpr int kSfaCol = 384;  // 4 columns: A scale factors (all 1.0)
@@ -48,24 +48,13 @@ struct __align__(1024) Smem {
   float ks[kScaleSlots][kTileM];       // per-position K scales
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
-  uint64_t t_full[6], t_empty[6];
+  uint64_t t_full[4], t_empty[4];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
   int g_begin, o_begin;
   long long t_begin, t_end;
   long long warp_sum[kThreads / 32];
-};
-
-// Ring position: slot index and phase parity, advanced one tile at a time.
-struct Ring {
-  uint32_t idx = 0, phase = 0;
-  __device__ __forceinline__ void next(uint32_t n) {
-    if (++idx == n) {
-      idx = 0;
-      phase ^= 1;
-    }
-  }
 };
 
 // Length that row `row` is scored over: L if it has more than skip_le_blocks
@@ -96,7 +85,7 @@ template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_amax8_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
   constexpr int N = 64 * R;                    // MMA N
-  constexpr int kNumAcc = 384 / N;             // accumulator stages
+  constexpr int kNumAcc = R == 3 ? 2 : 4;      // accumulator stages (power of two)
   constexpr int kEpiPerTile = R == 3 ? 3 : 1;  // epilogue warpgroups consuming each tile
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -188,8 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = sm.tmem_base;
   long long remaining = sm.t_end - sm.t_begin;
   int g = sm.g_begin, off = sm.o_begin;
-  Ring kr, sr, ar;      // same tile sequence on every role
-  uint32_t tseq = 0;    // tiles so far (decode: picks the epilogue warpgroup)
+  uint32_t tseq = 0;    // tiles so far: every ring slot and phase derives from it
   uint32_t issued = 0;  // TMA thread: tiles whose loads were issued
   const int epi = warp >= kEpiWarp0 ? (warp - kEpiWarp0) >> 2 : -1;  // epilogue warpgroup
   const int quad = warp & 3;
@@ -239,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (epi >= 0) {
       row = R == 3 ? g * 3 + epi : g;
       if (row < a.p.rows) {
-        rlen = max(scored_len(a, row), 0);
+        rlen = max(scored_len(a, row), 0);  // 0 when the row is skipped: nothing is stored
         const float4* wp = reinterpret_cast<const float4*>(a.p.w + static_cast<int64_t>(row) * kHeads);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -260,10 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const int req = a.p.layout == 1 ? 0 : g;
         const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
-        Ring k = kr, s = sr;
-        for (int t = off; t < off + take; ++t) {
-          if (!mbar_wait(&sm.k_empty[k.idx], k.phase ^ 1, abort_flag) ||
-              !mbar_wait(&sm.s_empty[s.idx], s.phase ^ 1, abort_flag)) {
+        uint32_t ts = tseq;
+        for (int t = off; t < off + take; ++t, ++ts) {
+          const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
+          const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+          if (!mbar_wait(&sm.k_empty[ki], kp ^ 1, abort_flag) || !mbar_wait(&sm.s_empty[si], sp ^ 1, abort_flag)) {
             set_abort(sm, a.p.dev_err);
             break;
           }
@@ -280,18 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++nvalid;
             }
           }
-          mbar_arrive_expect_tx(&sm.k_full[k.idx], nvalid * kPageValueBytes);
-          mbar_arrive_expect_tx(&sm.s_full[s.idx], nvalid * kPage * 4);
+          mbar_arrive_expect_tx(&sm.k_full[ki], nvalid * kPageValueBytes);
+          mbar_arrive_expect_tx(&sm.s_full[si], nvalid * kPage * 4);
           for (int j = 0; j < npages; ++j) {
             if (pid[j] < 0) continue;
-            tma_load_3d(sm.kv[k.idx] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[k.idx]);
-            bulk_load(&sm.ks[s.idx][j * kPage],
-                      a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, kPage * 4,
-                      &sm.s_full[s.idx]);
+            tma_load_3d(sm.kv[ki] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
+            bulk_load(&sm.ks[si][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes,
+                      kPage * 4, &sm.s_full[si]);
           }
           ++issued;
-          k.next(kStages);
-          s.next(kScaleSlots);
         }
       }
       __syncwarp();
@@ -305,24 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q) + 32 * k);
           idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, N, k, k);
         }
-        Ring k = kr, acc = ar;
-        for (int t = off; t < off + take; ++t) {
-          if (!mbar_wait(&sm.k_full[k.idx], k.phase, abort_flag) ||
-              !mbar_wait(&sm.t_empty[acc.idx], acc.phase ^ 1, abort_flag)) {
+        uint32_t ts = tseq;
+        for (int t = off; t < off + take; ++t, ++ts) {
+          const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
+          const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
+          if (!mbar_wait(&sm.k_full[ki], kp, abort_flag) || !mbar_wait(&sm.t_empty[ai], ap ^ 1, abort_flag)) {
             set_abort(sm, a.p.dev_err);
             break;
           }
           tc_fence_after();
-          const uint32_t d = tbase + acc.idx * N;
-          const uint32_t a0 = smem_u32(sm.kv[k.idx]);
+          const uint32_t d = tbase + ai * N;
+          const uint32_t a0 = smem_u32(sm.kv[ki]);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_mxf8f6f4(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol, tbase + kSfbCol,
                          kk);
-          mma_commit(&sm.k_empty[k.idx]);
-          mma_commit(&sm.t_full[acc.idx]);
-          k.next(kStages);
-          acc.next(kNumAcc);
+          mma_commit(&sm.k_empty[ki]);
+          mma_commit(&sm.t_full[ai]);
         }
       }
       __syncwarp();
@@ -332,18 +317,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nb = (rlen + kBlock - 1) / kBlock;
       float* keys_row = row >= 0 && row < a.p.rows ? a.keys + static_cast<int64_t>(row) * a.keys_stride : nullptr;
       const uint32_t col0 = R == 3 ? epi * kHeads : 0;
-      Ring s = sr, acc = ar;
-      uint32_t ts = tseq;
-      for (int t = off; t < off + take; ++t, ++ts, s.next(kScaleSlots), acc.next(kNumAcc)) {
+      const uint32_t ts0 = tseq;
+      float* kp_row = keys_row != nullptr ? keys_row + (p >> 3) : nullptr;  // + 16 t per tile
+      for (int t = off; t < off + take; ++t) {
+        const uint32_t ts = ts0 + (t - off);
         if (R == 1 && static_cast<int>(ts % 3) != epi) continue;
-        if (!warp_wait(&sm.t_full[acc.idx], acc.phase, abort_flag)) {
+        const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
+        const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+        if (!warp_wait_fast(&sm.t_full[ai], ap, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           break;
         }
         tc_fence_after();
         float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint32_t x[32];
-        const uint32_t taddr = tmem_addr(tbase, 32 * quad, acc.idx * N + col0);
+        const uint32_t taddr = tmem_addr(tbase, 32 * quad, ai * N + col0);
         tmem_ld32(taddr, x);
         tmem_ld_wait();
         head_reduce_half(part, x, w);
@@ -352,31 +340,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         head_reduce_half(part, x, w + 32);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.t_empty[acc.idx]);
+        if (lane == 0) mbar_arrive(&sm.t_empty[ai]);
         const float score = head_reduce_finish(part);
-        if (!warp_wait(&sm.s_full[s.idx], s.phase, abort_flag)) {
+        if (!warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           break;
         }
-        const float kscale = sm.ks[s.idx][p];
+        const float kscale = sm.ks[si][p];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_empty[s.idx]);
+        if (lane == 0) mbar_arrive(&sm.s_empty[si]);
         const int pos = t * kTileM + p;
-        const bool valid = keys_row != nullptr && pos < rlen;
-        float v = valid ? score * kscale : -__int_as_float(0x7f800000);
+        float v = pos < rlen ? score * kscale : -__int_as_float(0x7f800000);
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        if ((lane & 7) == 0 && valid) {
-          const int b = pos >> 3;
-          keys_row[b] = b == nb - 1 ? __int_as_float(0x7f800000) : v;
-        }
+        if ((lane & 7) == 0 && pos < rlen) kp_row[t * (kTileM / kBlock)] = (pos >> 3) == nb - 1 ? __int_as_float(0x7f800000) : v;
       }
-    }
-    for (int i = 0; i < take; ++i) {
-      kr.next(kStages);
-      sr.next(kScaleSlots);
-      ar.next(kNumAcc);
     }
     tseq += take;
     remaining -= take;

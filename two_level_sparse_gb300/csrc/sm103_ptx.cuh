@@ -175,6 +175,18 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Re-split the register file between warpgroups (all four warps of a
+// warpgroup execute it).  The block's total is threads x registers at launch;
+// the sizes chosen by a kernel must add up to no more than that.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor for a K-major operand laid out in 128-byte
 // swizzled rows (8-row atoms of 1024 B): start address, stride between 8-row
