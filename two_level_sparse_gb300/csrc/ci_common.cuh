@@ -82,6 +82,36 @@ __device__ __forceinline__ float head_reduce_finish(const float (&acc)[8]) {
   return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
+// ---------------------------------------------------------------- page ids of K tiles
+// The two pages (64 positions each) behind 128-position tile t of a request
+// whose page table is pt, for a scan over the first len positions: -1 where
+// the tile has no such position or where the id is out of range (reported).
+// A producer warp loads 32 tiles' ids at once (one tile per lane) one chunk
+// ahead of the tiles it issues, so no tile waits on a dependent global load.
+struct TilePages {
+  int lo, hi;
+};
+__device__ __forceinline__ TilePages load_tile_pages(const int32_t* pt, int t, int len, int64_t num_pages,
+                                                     int32_t* dev_err) {
+  TilePages r{-1, -1};
+  const int p0 = t * kTileM;
+  if (p0 < len) {
+    const int a = pt[2 * t];
+    const int b = p0 + kPage < len ? pt[2 * t + 1] : -1;
+    if (a < 0 || a >= num_pages)
+      report(dev_err, kDevErrPage);
+    else
+      r.lo = a;
+    if (p0 + kPage < len) {
+      if (b < 0 || b >= num_pages)
+        report(dev_err, kDevErrPage);
+      else
+        r.hi = b;
+    }
+  }
+  return r;
+}
+
 // ---------------------------------------------------------------- ordering keys
 // Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 maps
 // like +0.  Every finite score and -inf map above 0, which marks "no entry".

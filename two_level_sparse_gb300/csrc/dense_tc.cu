@@ -245,42 +245,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA producer
-      if (lane == 0) {
-        const int req = a.p.layout == 1 ? 0 : g;
-        const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
-        uint32_t ts = tseq;
-        for (int t = off; t < off + take; ++t, ++ts) {
-          const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
-          const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
-          if (!mbar_wait(&sm.k_empty[ki], kp ^ 1, abort_flag) || !mbar_wait(&sm.s_empty[si], sp ^ 1, abort_flag)) {
-            set_abort(sm, a.p.dev_err);
-            break;
-          }
-          const int npos = min(kTileM, glen - t * kTileM);
-          const int npages = (npos + kPage - 1) / kPage;
-          int pid[2] = {-1, -1};
-          uint32_t nvalid = 0;
-          for (int j = 0; j < npages; ++j) {
-            const int p = pt[t * 2 + j];
-            if (p < 0 || p >= a.p.num_pages) {
-              report(a.p.dev_err, kDevErrPage);
+      const int req = a.p.layout == 1 ? 0 : g;
+      const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
+      const int end = off + take;
+      uint32_t ts = tseq;
+      bool ok = true;
+      TilePages nxt{-1, -1};
+      if (off + lane < end) nxt = load_tile_pages(pt, off + lane, glen, a.p.num_pages, a.p.dev_err);
+      for (int c0 = off; c0 < end && ok; c0 += 32) {
+        const TilePages cur = nxt;
+        if (c0 + 32 + lane < end) nxt = load_tile_pages(pt, c0 + 32 + lane, glen, a.p.num_pages, a.p.dev_err);
+        const int n = min(32, end - c0);
+        for (int i = 0; i < n; ++i, ++ts) {
+          const int pid[2] = {__shfl_sync(0xffffffffu, cur.lo, i), __shfl_sync(0xffffffffu, cur.hi, i)};
+          if (lane == 0) {
+            const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
+            const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+            if (!mbar_wait(&sm.k_empty[ki], kp ^ 1, abort_flag) || !mbar_wait(&sm.s_empty[si], sp ^ 1, abort_flag)) {
+              set_abort(sm, a.p.dev_err);
+              ok = false;
             } else {
-              pid[j] = p;
-              ++nvalid;
+              const uint32_t nvalid = (pid[0] >= 0) + (pid[1] >= 0);
+              mbar_arrive_expect_tx(&sm.k_full[ki], nvalid * kPageValueBytes);
+              mbar_arrive_expect_tx(&sm.s_full[si], nvalid * kPage * 4);
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                if (pid[j] < 0) continue;
+                tma_load_3d(sm.kv[ki] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
+                bulk_load(&sm.ks[si][j * kPage],
+                          a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, kPage * 4,
+                          &sm.s_full[si]);
+              }
+              ++issued;
             }
           }
-          mbar_arrive_expect_tx(&sm.k_full[ki], nvalid * kPageValueBytes);
-          mbar_arrive_expect_tx(&sm.s_full[si], nvalid * kPage * 4);
-          for (int j = 0; j < npages; ++j) {
-            if (pid[j] < 0) continue;
-            tma_load_3d(sm.kv[ki] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
-            bulk_load(&sm.ks[si][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes,
-                      kPage * 4, &sm.s_full[si]);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+            ok = false;
+            break;
           }
-          ++issued;
         }
       }
-      __syncwarp();
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
       if (lane == 0) {
