@@ -258,63 +258,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = min(32, end - c0);
         for (int i = 0; i < n; ++i, ++ts) {
           const int pid[2] = {__shfl_sync(0xffffffffu, cur.lo, i), __shfl_sync(0xffffffffu, cur.hi, i)};
-          if (lane == 0) {
-            const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
-            const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
-            if (!mbar_wait(&sm.k_empty[ki], kp ^ 1, abort_flag) || !mbar_wait(&sm.s_empty[si], sp ^ 1, abort_flag)) {
-              set_abort(sm, a.p.dev_err);
-              ok = false;
-            } else {
-              const uint32_t nvalid = (pid[0] >= 0) + (pid[1] >= 0);
-              mbar_arrive_expect_tx(&sm.k_full[ki], nvalid * kPageValueBytes);
-              mbar_arrive_expect_tx(&sm.s_full[si], nvalid * kPage * 4);
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                if (pid[j] < 0) continue;
-                tma_load_3d(sm.kv[ki] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
-                bulk_load(&sm.ks[si][j * kPage],
-                          a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, kPage * 4,
-                          &sm.s_full[si]);
-              }
-              ++issued;
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
+          const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+          if (!warp_wait_fast(&sm.k_empty[ki], kp ^ 1, abort_flag) ||
+              !warp_wait_fast(&sm.s_empty[si], sp ^ 1, abort_flag)) {
+            if (lane == 0) set_abort(sm, a.p.dev_err);
             ok = false;
             break;
           }
+          const uint32_t nvalid = (pid[0] >= 0) + (pid[1] >= 0);
+          mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * kPageValueBytes);
+          mbar_arrive_expect_tx_elect(&sm.s_full[si], nvalid * kPage * 4);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (pid[j] < 0) continue;
+            tma_load_3d_elect(sm.kv[ki] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
+            bulk_load_elect(&sm.ks[si][j * kPage],
+                            a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, kPage * 4,
+                            &sm.s_full[si]);
+          }
+          ++issued;
         }
       }
     } else if (warp == 1) {
-      // ---------------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        uint64_t bdesc[4];
-        uint32_t idesc[4];
+      // ---------------------------------------------------------------- MMA issuer (whole warp, one lane issues)
+      uint64_t bdesc[4];
+      uint32_t idesc[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q) + 32 * k);
-          idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, N, k, k);
-        }
-        uint32_t ts = tseq;
-        for (int t = off; t < off + take; ++t, ++ts) {
-          const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
-          const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
-          if (!mbar_wait(&sm.k_full[ki], kp, abort_flag) || !mbar_wait(&sm.t_empty[ai], ap ^ 1, abort_flag)) {
-            set_abort(sm, a.p.dev_err);
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d = tbase + ai * N;
-          const uint32_t a0 = smem_u32(sm.kv[ki]);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_mxf8f6f4(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol, tbase + kSfbCol,
-                         kk);
-          mma_commit(&sm.k_empty[ki]);
-          mma_commit(&sm.t_full[ai]);
-        }
+      for (int k = 0; k < 4; ++k) {
+        bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q) + 32 * k);
+        idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, N, k, k);
       }
-      __syncwarp();
+      uint32_t ts = tseq;
+      for (int t = off; t < off + take; ++t, ++ts) {
+        const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
+        const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
+        if (!warp_wait_fast(&sm.k_full[ki], kp, abort_flag) || !warp_wait_fast(&sm.t_empty[ai], ap ^ 1, abort_flag)) {
+          if (lane == 0) set_abort(sm, a.p.dev_err);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tbase + ai * N;
+        const uint32_t a0 = smem_u32(sm.kv[ki]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol,
+                             tbase + kSfbCol, kk);
+        mma_commit_elect(&sm.k_empty[ki]);
+        mma_commit_elect(&sm.t_full[ai]);
+      }
     } else if (epi >= 0) {
       // ---------------------------------------------------------------- epilogue
       const int p = 32 * quad + lane;
