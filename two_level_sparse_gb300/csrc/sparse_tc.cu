@@ -357,54 +357,52 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
 
   const int rows = a.p.rows;
   if (warp == 0) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      Ring kr, ar;
-      int ri = 0;
-      bool ok = true;
-      for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
-        const RowInfo r = row_info(a, row, true);
-        const int b = ri & 1;
-        if (!mbar_wait(&sm.q_full[b], (ri >> 1) & 1, abort_flag)) {
+    // ------------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
+    Ring kr, ar;
+    int ri = 0;
+    bool ok = true;
+    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
+      const RowInfo r = row_info(a, row, lane == 0);
+      const int b = ri & 1;
+      if (!warp_wait_fast(&sm.q_full[b], (ri >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sfb = tbase + kSfbCol + 4 * b;
+      tmem_cp_32x128b_x4_elect(sfb, sdesc_rows16(smem_u32(sm.sf[b])));
+      uint64_t bdesc[4];
+      uint32_t idesc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q[b]) + 32 * k);
+        idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
+      }
+      for (int t = 0; t < r.ntiles; ++t) {
+        if (!warp_wait_fast(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
+            !warp_wait_fast(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
+        fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
         tc_fence_after();
-        const uint32_t sfb = tbase + kSfbCol + 4 * b;
-        tmem_cp_32x128b_x4(sfb, sdesc_rows16(smem_u32(sm.sf[b])));
-        uint64_t bdesc[4];
-        uint32_t idesc[4];
+        const uint32_t d = tbase + ar.idx * kHeads;
+        const uint32_t a0 = smem_u32(sm.kv[kr.idx]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q[b]) + 32 * k);
-          idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
-        }
-        for (int t = 0; t < r.ntiles; ++t) {
-          if (!mbar_wait(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
-              !mbar_wait(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
-          tc_fence_after();
-          const uint32_t d = tbase + ar.idx * kHeads;
-          const uint32_t a0 = smem_u32(sm.kv[kr.idx]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_mxf8f6f4(d, sdesc_k128_sw128(a0 + 32 * k), bdesc[k], idesc[k], tbase + kSfaCol, sfb, k);
-          mma_commit(&sm.k_empty[kr.idx]);
-          mma_commit(&sm.t_full[ar.idx]);
-          kr.next(kStages);
-          ar.next(kNumAcc);
-        }
-        if (ok) mma_commit(&sm.q_empty[b]);  // the query buffer is free once these MMAs complete
+        for (int k = 0; k < 4; ++k)
+          mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * k), bdesc[k], idesc[k], tbase + kSfaCol, sfb, k);
+        mma_commit_elect(&sm.k_empty[kr.idx]);
+        mma_commit_elect(&sm.t_full[ar.idx]);
+        kr.next(kStages);
+        ar.next(kNumAcc);
       }
-      if (!ok) set_abort(sm, a.p.dev_err);
+      if (ok) mma_commit_elect(&sm.q_empty[b]);  // the query buffer is free once these MMAs complete
     }
-    __syncwarp();
+    if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
     // ------------------------------------------------------------------ gather
     const int gw = warp - kGatherWarp0;
+    const uint32_t dst0 = sw128_offset(lane >> 3, (lane & 7) * 16), dst1 = sw128_offset(4 + (lane >> 3), (lane & 7) * 16);
     Ring kr, sr;
     int ri = 0;
     bool ok = true;
@@ -429,17 +427,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
                            (((v >> 4) & 7) * kBlock + half * 4) * 4);
           cp_async_arrive_noinc(&sm.s_full[sr.idx]);
         }
+        // block blk of the tile: 1 KB contiguous in its page -> one 8-row swizzle atom;
+        // lane l copies 16-byte chunks l and l + 32 (rows l / 8 and 4 + l / 8)
         uint8_t* dst = sm.kv[kr.idx];
-#pragma unroll 4
-        for (int j = gw; j < 32; j += kGatherWarps) {
-          const int blk = j >> 1;  // instruction j: 512 contiguous bytes of block j / 2
-          const int slot = t * kBlocksPerTile + blk;
+        const int row_base = t * kBlocksPerTile;
+#pragma unroll 2
+        for (int blk = gw; blk < kBlocksPerTile; blk += kGatherWarps) {
+          const int slot = row_base + blk;
           const int v = slot < r.nv ? info[slot] : -1;
           if (v >= 0) {
-            const int o = (j & 1) * 32 + lane;  // 16-byte chunk of the block's 1 KB
             const uint8_t* src =
-                a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + ((v >> 4) & 7) * (kBlock * kDim) + o * 16;
-            cp_async16(dst + sw128_offset(blk * kBlock + (o >> 3), (o & 7) * 16), src);
+                a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + ((v >> 4) & 7) * (kBlock * kDim) + lane * 16;
+            cp_async16(dst + blk * (kBlock * kDim) + dst0, src);
+            cp_async16(dst + blk * (kBlock * kDim) + dst1, src + 512);
           }
         }
         cp_async_arrive_noinc(&sm.k_full[kr.idx]);
