@@ -46,7 +46,8 @@ constexpr int kScoreCol = 208;    // two buffers of kMaxTiles score columns
 constexpr int kBlocksPerTile = kTileM / kBlock;  // 16
 constexpr int kMaxBlocks = 2176;                 // >= topk + 1 for every supported topk
 constexpr int kMaxTiles = kMaxBlocks / kBlocksPerTile;  // 136
-constexpr int kGatherWarp0 = 1, kGatherWarps = 3;
+constexpr int kGatherWarp0 = 1, kGatherWarps = 3;  // warp 1 tensor-map loads, warps 2-3 cp.async
+constexpr int kTmaBlocks = 8;  // blocks of a tile fetched by tensor-map loads (the rest by cp.async)
 constexpr int kTopkWarp0 = 4, kTopkThreads = 128, kTopkBar = 2;  // also the next-row prep
 constexpr int kPrepThreads = kTopkThreads;
 constexpr int kScoreWarp0 = 8;
@@ -61,7 +62,7 @@ struct __align__(1024) Smem {
   // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
   int32_t info[2][kMaxBlocks];
   uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
-  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t k_full[kStages], tk_full[kStages], k_empty[kStages];
   uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
   uint64_t t_full[kNumAcc], t_empty[kNumAcc];
   uint64_t q_full[2], q_empty[2];
@@ -306,7 +307,8 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    select_kernel(const __grid_constant__ CUtensorMap tmap, const SelectArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -318,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
   }
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], 32 * kGatherWarps);  // one cp.async-tracked arrival per gather lane
+      mbar_init(&sm.k_full[s], 32 * (kGatherWarps - 1));  // one cp.async-tracked arrival per copying lane
+      mbar_init(&sm.tk_full[s], 1);                       // the tensor-map loads (transaction bytes)
       mbar_init(&sm.k_empty[s], 1);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
@@ -341,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&tmap);
   }
   tc_fence_before();
   __syncthreads();
@@ -380,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
       }
       for (int t = 0; t < r.ntiles; ++t) {
         if (!warp_wait_fast(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
+            !warp_wait_fast(&sm.tk_full[kr.idx], kr.phase, abort_flag) ||
             !warp_wait_fast(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -401,10 +406,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
     // ------------------------------------------------------------------ gather
+    // Random 1 KB gathers from L2 are capped per path: tensor-map loads by the
+    // rate one warp can issue them, cp.async by the copies the load/store unit
+    // keeps in flight.  Both paths run side by side: warp 1 issues tensor-map
+    // loads for the first kTmaBlocks blocks of a tile (one 8-row box each,
+    // landing on its own swizzle atom), warps 2-3 copy the other blocks with
+    // 16-byte cp.async, and warp 2 also copies the K scales.
     const int gw = warp - kGatherWarp0;
     const uint32_t dst0 = sw128_offset(lane >> 3, (lane & 7) * 16), dst1 = sw128_offset(4 + (lane >> 3), (lane & 7) * 16);
     Ring kr, sr;
     int ri = 0;
+    uint32_t issued = 0;  // warp 1: tiles whose tensor-map loads were issued
     bool ok = true;
     for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
       const RowInfo r = row_info(a, row, false);
@@ -412,42 +424,62 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
       ok = warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t) {
-        if ((gw == 0 && !warp_wait(&sm.s_empty[sr.idx], sr.phase ^ 1, abort_flag)) ||
+        if ((gw == 1 && !warp_wait(&sm.s_empty[sr.idx], sr.phase ^ 1, abort_flag)) ||
             !warp_wait(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        if (gw == 0) {  // scales: lane l copies half of block l / 2's eight fp32 scales
-          const int blk = lane >> 1, half = lane & 1;
-          const int slot = t * kBlocksPerTile + blk;
-          const int v = slot < r.nv ? info[slot] : -1;
-          if (v >= 0)
-            cp_async16(&sm.ks[sr.idx][blk * kBlock + half * 4],
-                       a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + kPageValueBytes +
-                           (((v >> 4) & 7) * kBlock + half * 4) * 4);
-          cp_async_arrive_noinc(&sm.s_full[sr.idx]);
-        }
-        // block blk of the tile: 1 KB contiguous in its page -> one 8-row swizzle atom;
-        // lane l copies 16-byte chunks l and l + 32 (rows l / 8 and 4 + l / 8)
         uint8_t* dst = sm.kv[kr.idx];
         const int row_base = t * kBlocksPerTile;
-#pragma unroll 2
-        for (int blk = gw; blk < kBlocksPerTile; blk += kGatherWarps) {
-          const int slot = row_base + blk;
-          const int v = slot < r.nv ? info[slot] : -1;
-          if (v >= 0) {
-            const uint8_t* src =
-                a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + ((v >> 4) & 7) * (kBlock * kDim) + lane * 16;
-            cp_async16(dst + blk * (kBlock * kDim) + dst0, src);
-            cp_async16(dst + blk * (kBlock * kDim) + dst1, src + 512);
+        if (gw == 0) {
+          const int slot = row_base + lane;
+          const int v = lane < kTmaBlocks && slot < r.nv ? info[slot] : -1;
+          const uint32_t live = __ballot_sync(0xffffffffu, v >= 0);
+          mbar_arrive_expect_tx_elect(&sm.tk_full[kr.idx], __popc(live) * (kBlock * kDim));
+#pragma unroll
+          for (int blk = 0; blk < kTmaBlocks; ++blk) {
+            const int vb = __shfl_sync(0xffffffffu, v, blk);
+            if (vb >= 0)
+              tma_load_3d_elect(dst + blk * (kBlock * kDim), &tmap, 0, ((vb >> 4) & 7) * kBlock, vb >> 7,
+                                &sm.tk_full[kr.idx]);
           }
+          ++issued;
+        } else {
+          if (gw == 1) {  // scales: lane l copies half of block l / 2's eight fp32 scales
+            const int blk = lane >> 1, half = lane & 1;
+            const int slot = row_base + blk;
+            const int v = slot < r.nv ? info[slot] : -1;
+            if (v >= 0)
+              cp_async16(&sm.ks[sr.idx][blk * kBlock + half * 4],
+                         a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + kPageValueBytes +
+                             (((v >> 4) & 7) * kBlock + half * 4) * 4);
+            cp_async_arrive_noinc(&sm.s_full[sr.idx]);
+          }
+          // block blk: 1 KB contiguous in its page -> one 8-row swizzle atom;
+          // lane l copies 16-byte chunks l and l + 32 (rows l / 8 and 4 + l / 8)
+#pragma unroll 2
+          for (int blk = kTmaBlocks + gw - 1; blk < kBlocksPerTile; blk += kGatherWarps - 1) {
+            const int slot = row_base + blk;
+            const int v = slot < r.nv ? info[slot] : -1;
+            if (v >= 0) {
+              const uint8_t* src = a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes +
+                                   ((v >> 4) & 7) * (kBlock * kDim) + lane * 16;
+              cp_async16(dst + blk * (kBlock * kDim) + dst0, src);
+              cp_async16(dst + blk * (kBlock * kDim) + dst1, src + 512);
+            }
+          }
+          cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         }
-        cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         kr.next(kStages);
         sr.next(kScaleSlots);
       }
       __syncwarp();
       if (ok) mbar_arrive(&sm.info_empty[b]);
+    }
+    if (gw == 0 && !ok && lane == 0) {
+      // no tensor-map load may still be writing when the CTA exits
+      for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        mbar_wait(&sm.tk_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
     }
     cp_async_wait<0>();
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
@@ -604,8 +636,11 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   const int smem = static_cast<int>(select_smem_bytes(a.max_blocks));
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  CUtensorMap tmap;
+  e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, kBlock);
+  if (e != cudaSuccess) return e;
   const int grid = min(device_sm_count(), a.p.rows);
-  select_kernel<<<grid, kThreads, smem, stream>>>(a);
+  select_kernel<<<grid, kThreads, smem, stream>>>(tmap, a);
   return cudaGetLastError();
 }
 
