@@ -62,6 +62,8 @@ struct __align__(1024) Smem {
   // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
   int32_t info[2][kMaxBlocks];
   uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
+  int gbase[kMaxTiles], ebase[kMaxTiles];  // top-k: entries above / at the threshold before each tile
+  int scan_part[2][kTopkThreads / 32];
   uint64_t k_full[kStages], tk_full[kStages], k_empty[kStages];
   uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
   uint64_t t_full[kNumAcc], t_empty[kNumAcc];
@@ -278,8 +280,82 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
     }
   }
   named_sync(kTopkBar, kTopkThreads);
+  // Entries above / at the threshold in the tiles before each tile: thread kt
+  // counts tiles kt and kt + 128, then a block-wide exclusive scan.
+  {
+    int g0 = 0, e0 = 0, g1 = 0, e1 = 0;
+    if (kt < nt) {
+      const uint4 g4 = sm.mgt[kt], e4 = sm.meq[kt];
+      g0 = __popc(g4.x) + __popc(g4.y) + __popc(g4.z) + __popc(g4.w);
+      e0 = __popc(e4.x) + __popc(e4.y) + __popc(e4.z) + __popc(e4.w);
+    }
+    if (kt + kTopkThreads < nt) {
+      const uint4 g4 = sm.mgt[kt + kTopkThreads], e4 = sm.meq[kt + kTopkThreads];
+      g1 = __popc(g4.x) + __popc(g4.y) + __popc(g4.z) + __popc(g4.w);
+      e1 = __popc(e4.x) + __popc(e4.y) + __popc(e4.z) + __popc(e4.w);
+    }
+    // first 128 tiles, then the rest, each scanned across the block
+    int gi = g0, ei = e0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int gv = __shfl_up_sync(0xffffffffu, gi, o), ev = __shfl_up_sync(0xffffffffu, ei, o);
+      if (l >= o) {
+        gi += gv;
+        ei += ev;
+      }
+    }
+    if (l == 31) {
+      sm.scan_part[0][q] = gi;
+      sm.scan_part[1][q] = ei;
+    }
+    int gj = g1, ej = e1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int gv = __shfl_up_sync(0xffffffffu, gj, o), ev = __shfl_up_sync(0xffffffffu, ej, o);
+      if (l >= o) {
+        gj += gv;
+        ej += ev;
+      }
+    }
+    named_sync(kTopkBar, kTopkThreads);
+    int gw_before = 0, ew_before = 0, gtot = 0, etot = 0;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+      const int gs = sm.scan_part[0][w], es = sm.scan_part[1][w];
+      if (w < q) {
+        gw_before += gs;
+        ew_before += es;
+      }
+      gtot += gs;
+      etot += es;
+    }
+    named_sync(kTopkBar, kTopkThreads);
+    if (l == 31) {
+      sm.scan_part[0][q] = gj;
+      sm.scan_part[1][q] = ej;
+    }
+    named_sync(kTopkBar, kTopkThreads);
+    int gw2 = 0, ew2 = 0;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w)
+      if (w < q) {
+        gw2 += sm.scan_part[0][w];
+        ew2 += sm.scan_part[1][w];
+      }
+    if (kt < nt) {
+      sm.gbase[kt] = gw_before + gi - g0;
+      sm.ebase[kt] = ew_before + ei - e0;
+    }
+    if (kt + kTopkThreads < nt) {
+      sm.gbase[kt + kTopkThreads] = gtot + gw2 + gj - g1;
+      sm.ebase[kt + kTopkThreads] = etot + ew2 + ej - e1;
+    }
+  }
+  named_sync(kTopkBar, kTopkThreads);
+  // Emit: only the tiles where this lane holds a selected entry cost more than
+  // two compares.  Rank = entries above the threshold before it + entries at
+  // the threshold before it (capped at need_eq), in (tile, position) order.
   const uint32_t lt = lanemask_lt();
-  uint32_t run_gt = 0, run_eq = 0;
   for (int c0 = 0; c0 < nt; c0 += 32) {
     tmem_ld32(lane_col0 + c0, x);
     tmem_ld_wait();
@@ -287,22 +363,20 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
     for (int j = 0; j < 32; ++j) {
       const int t = c0 + j;
       if (t >= nt) break;
+      const uint32_t m = x[j] & mask;
+      const bool is_gt = m > prefix, is_eq = m == prefix;
+      if (!(is_gt || is_eq)) continue;
       const uint4 g4 = sm.mgt[t], e4 = sm.meq[t];
       const uint32_t g[4] = {g4.x, g4.y, g4.z, g4.w}, e[4] = {e4.x, e4.y, e4.z, e4.w};
-      uint32_t gtb = run_gt, eqb = run_eq;
+      uint32_t gtb = static_cast<uint32_t>(sm.gbase[t]) + __popc(g[q] & lt);
+      uint32_t eqb = static_cast<uint32_t>(sm.ebase[t]) + __popc(e[q] & lt);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < 4; ++w)
         if (w < q) {
           gtb += __popc(g[w]);
           eqb += __popc(e[w]);
         }
-        run_gt += __popc(g[w]);
-        run_eq += __popc(e[w]);
-      }
-      const bool is_gt = (g[q] >> l) & 1u, is_eq = (e[q] >> l) & 1u;
-      const uint32_t eq_rank = eqb + __popc(e[q] & lt);
-      if (is_gt || (is_eq && eq_rank < need_eq))
-        emit(static_cast<int>(gtb + __popc(g[q] & lt) + min(eq_rank, need_eq)), t, kt, x[j]);
+      if (is_gt || eqb < need_eq) emit(static_cast<int>(gtb + min(eqb, need_eq)), t, kt, x[j]);
     }
   }
 }
