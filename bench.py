@@ -120,30 +120,56 @@ def algorithmic_counts(wl):
     return flops, kbytes + qbytes, positions
 
 
-def time_steps(step, steps, warmup, flush, stream, dense_events=True):
-    """Per-step and per-dense-kernel CUDA-event durations (ms) on `stream`."""
-    from two_level_sparse_gb300 import ci
+def select_bytes(wl):
+    """Algorithmic bytes of the step's five sparse-scorer launches.
 
-    wl = step.wl
+    Per candidate position 132 bytes (128 e4m3 + one fp32 scale) gathered; per
+    row and launch the query, its scales and weights (4608 bytes), the block
+    ids (4 per block) and the output positions (4 per pick).  A row with
+    nb_t <= K' blocks scores all L_t positions; otherwise K' - 1 full blocks
+    plus its newest (partial) block.  The source runs with K' = P + 1 blocks,
+    each consumer with K.
+    """
+    L = wl.seq_len.to(torch.int64).cpu()
+    nb = (L + 7) // 8
+    P, K = wl.topk, wl.topk_blocks
+
+    def one(kb):
+        full = nb > kb
+        pos = torch.where(full, 8 * (kb - 1) + (L - 8 * (nb - 1)), L)
+        blocks = torch.where(full, torch.full_like(nb, kb), nb)
+        return int((132 * pos + 4608 + 4 * blocks + 4 * P).sum())
+
+    return one(P + 1) + (len(wl.layers) - 1) * one(K)
+
+
+def time_steps(step, steps, warmup, flush, stream, dense_events=True):
+    """Per-step CUDA-event durations (ms) on `stream`, whole step and per
+    kernel kind (events recorded between the step's launches)."""
     for _ in range(warmup):
         step.run(stream)
     torch.cuda.synchronize()
-    t_step, t_dense = [], []
+    out = {"step": [], "dense": [], "publish": [], "select": []}
     for _ in range(steps):
         with torch.cuda.stream(stream):
             flush.zero_()  # evict L2 between steps (same stream, before the first event: not timed)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        ev[0].record(stream)
-        src = wl.layers[0]
-        ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, wl.page_table, wl.layout, wl.seq_len,
-                                step.max_len, step.skip, step.keys, dev_err=step.dev_err, stream=stream)
-        ev[1].record(stream)
-        step.run_after_dense(stream)
-        ev[2].record(stream)
+        marks = []
+
+        def mark(name):
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            marks.append((name, ev))
+
+        mark("start")
+        step.run(stream, mark=mark)
         torch.cuda.synchronize()
-        t_dense.append(ev[0].elapsed_time(ev[1]))
-        t_step.append(ev[0].elapsed_time(ev[2]))
-    return t_step, t_dense
+        per = {"dense": 0.0, "publish": 0.0, "select": 0.0}
+        for (_, a), (name, b) in zip(marks, marks[1:]):
+            per[name] += a.elapsed_time(b)
+        out["step"].append(marks[0][1].elapsed_time(marks[-1][1]))
+        for k, v in per.items():
+            out[k].append(v)
+    return out
 
 
 def e2e_time(step, host_inputs, steps, stream):
@@ -238,25 +264,6 @@ def run_reference(args):
     return 0
 
 
-class BenchStep:
-    """IndexerStep whose dense launch can be timed separately."""
-
-    def __init__(self, wl):
-        from two_level_sparse_gb300.step import IndexerStep
-
-        self.inner = IndexerStep(wl)
-        self.wl = wl
-
-    def __getattr__(self, k):
-        return getattr(self.inner, k)
-
-    def run(self, stream=None):
-        self.inner.run(stream)
-
-    def run_after_dense(self, stream=None):
-        self.inner.run(stream, skip_dense=True)
-
-
 def last_rows(wl, rows):
     from two_level_sparse_gb300 import synth
 
@@ -273,15 +280,17 @@ def last_rows(wl, rows):
 def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0):
     from two_level_sparse_gb300 import synth
 
+    from two_level_sparse_gb300.step import IndexerStep
+
     wl = last_rows(synth.config_workload(cid, device="cuda"), rows)
-    step = BenchStep(wl)
-    t_step, t_dense = time_steps(step, steps, warmup, flush, stream)
-    res = {"cid": cid, "wl": wl, "step": step, "t_step": t_step, "t_dense": t_dense,
-           "launches": step.inner.launches()}
+    step = IndexerStep(wl)
+    times = time_steps(step, steps, warmup, flush, stream)
+    res = {"cid": cid, "wl": wl, "step": step, "t_step": times["step"], "t_dense": times["dense"],
+           "t_select": times["select"], "t_publish": times["publish"], "launches": step.launches()}
     if e2e:
         host = [t.cpu().pin_memory() for t in [wl.seq_len, wl.page_table] +
                 [x for l in wl.layers for x in (l.q_fp4, l.q_sf, l.w, l.k_pool)]]
-        res["e2e"] = e2e_time(step.inner, host, max(2, min(steps, 5)), stream)
+        res["e2e"] = e2e_time(step, host, max(2, min(steps, 5)), stream)
     return res
 
 
@@ -326,15 +335,20 @@ def main():
         wall = time.perf_counter() - t0
     ms_step = statistics.mean(head["t_step"])
     ms_dense = statistics.mean(head["t_dense"])
+    ms_select = statistics.mean(head["t_select"])
+    ms_publish = statistics.mean(head["t_publish"])
     if world > 1:
-        t = torch.tensor([ms_step, ms_dense], device="cuda")
+        t = torch.tensor([ms_step, ms_dense, ms_select, ms_publish], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, ms_dense = t.tolist()
+        ms_step, ms_dense, ms_select, ms_publish = t.tolist()
     wl = head["wl"]
     err = int(head["step"].dev_err.item())
     flops, kbytes, positions = algorithmic_counts(wl)
     fp8_peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     achieved = flops / (ms_dense * 1e-3) / 1e12
+    sel_bytes = select_bytes(wl)
+    n_select = len(wl.layers)
+    sel_gbs = sel_bytes / (ms_select * 1e-3) / 1e9
     e2e_ms, h2d, d2h = head.get("e2e", ([float("nan")], 0, 0))
     e2e_val = statistics.mean(e2e_ms)
     if world > 1:
@@ -374,10 +388,19 @@ def main():
         "config": {"workload": wl.name, "rows": wl.rows, "context": wl.max_len,
                    "topk_blocks": 2048, "topk": 512, "layers": 5, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MiB write)"},
-        "roofline": {"bound": "tensor", "kernel": "dense_amax8_kernel", "achieved": achieved, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained x2 (fp8 / bf16 nominal ratio)",
-                     "flops_per_launch": flops, "dense_ms": ms_dense},
+        "roofline": {"bound": "hbm", "kernel": "select_kernel", "achieved": sel_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": sel_gbs / peaks["hbm_gbs"],
+                     "traffic": select_traffic(),
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "bytes_per_launch": sel_bytes / n_select, "launches_per_step": n_select,
+                     "ms_per_launch": ms_select / n_select,
+                     "note": "candidate K gathered per launch (132 B per position) / mean launch time; "
+                             "for a prefill chunk the 34.6 MB pool per layer is L2-resident"},
+        "dense_roofline": {"bound": "tensor", "kernel": "dense_amax8_kernel", "achieved": achieved, "peak": fp8_peak,
+                           "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                           "peak_source": f"{peak_src} bf16_tflops_sustained x2 (fp8 / bf16 nominal ratio)",
+                           "flops_per_launch": flops, "ms_per_launch": ms_dense},
+        "kernel_ms": {"dense": ms_dense, "publish": ms_publish, "select": ms_select},
         "e2e": {"value": e2e_val / world, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": head_launches(args.steps, world),
         "clocks": clk.summary(),
@@ -393,6 +416,28 @@ def main():
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+# DRAM bytes (read + write) per launch of the sparse scorer, from an ncu
+# capture of a consumer-layer launch of the headline chunk, with the hash of
+# the kernel sources it was taken on; reported only while they still match.
+SELECT_TRAFFIC = {"bytes_per_launch": None, "sources_sha256": None}
+
+
+def _select_sources_sha():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "two_level_sparse_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def select_traffic():
+    if SELECT_TRAFFIC["bytes_per_launch"] is None or SELECT_TRAFFIC["sources_sha256"] != _select_sources_sha():
+        return None
+    return SELECT_TRAFFIC["bytes_per_launch"]
 
 
 def head_launches(steps, world):

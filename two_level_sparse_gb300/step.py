@@ -56,10 +56,12 @@ class IndexerStep:
         """Kernels one run() enqueues."""
         return 1 + (1 if self.Kp == self.K else 2) + len(self.wl.layers)
 
-    def run(self, stream=None, skip_dense=False):
+    def run(self, stream=None, skip_dense=False, mark=None):
         """Enqueue the step on `stream` (default: torch's current stream).
         ``skip_dense`` leaves out the first call, for callers that enqueue it
-        themselves (the benchmark times it on its own)."""
+        themselves.  ``mark(name)``, if given, is called after each launch is
+        enqueued (the benchmark records a CUDA event there)."""
+        mark = mark or (lambda name: None)
         wl = self.wl
         src = wl.layers[0]
         common = dict(page_table=wl.page_table, layout=wl.layout, seq_len=wl.seq_len, max_len=self.max_len,
@@ -67,17 +69,21 @@ class IndexerStep:
         if not skip_dense:
             ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, skip_le_blocks=self.skip, keys=self.keys,
                                     **common)
+            mark("dense")
         ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
                              dev_err=self.dev_err, stream=stream)
+        mark("publish")
         if self.Kp != self.K:
             ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.Kp, self.blocks_src, self.nvalid_src,
                                  dev_err=self.dev_err, stream=stream)
+            mark("publish")
         for j, layer in enumerate(wl.layers):
             blocks, nvalid, mb = (self.blocks_src, self.nvalid_src, self.Kp) if j == 0 else (self.blocks,
                                                                                             self.nvalid, self.K)
             ci.ci_select_sparse(layer.q_fp4, layer.q_sf, layer.w, layer.k_pool, blocks=blocks, nvalid=nvalid,
                                 max_blocks=mb, topk=self.P, out_pos=self.pos[j],
                                 out_score=None if self.score is None else self.score[j], **common)
+            mark("select")
 
     def outputs_numpy(self):
         out = dict(keys=self.keys.cpu().numpy(), blocks=self.blocks.cpu().numpy(), nvalid=self.nvalid.cpu().numpy(),
