@@ -68,15 +68,28 @@ __device__ __forceinline__ bool warp_wait_fast(uint64_t* bar, uint32_t parity, v
   return warp_wait(bar, parity, abort);
 }
 
+// Two IEEE round-to-nearest fused multiply-adds in one packed instruction
+// (a_i = w_i * r_i + a_i for i = 0, 1; the same results as two fmaf calls).
+__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float w0, float w1, float r0, float r1) {
+  asm("{\n\t.reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
+      "fma.rn.f32x2 a, b, c, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(r0), "f"(r1));
+}
+
 // ---------------------------------------------------------------- score epilogue
 // Head-weighted ReLU reduction of one (row, position) pair from its 64 fp32
 // accumulator columns, delivered in two halves of 32: eight partial sums
 // (head h feeds partial h % 8), combined in a fixed tree.  Every kernel that
 // scores a position uses this function, so identical K vectors give
-// bit-identical scores wherever they are scored.
+// bit-identical scores wherever they are scored.  Pairs of heads go through
+// one packed FMA (adjacent partial sums).
 __device__ __forceinline__ void head_reduce_half(float (&acc)[8], const uint32_t (&x)[32], const float* w) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j & 7] = fmaf(w[j], fmaxf(__uint_as_float(x[j]), 0.0f), acc[j & 7]);
+  for (int j = 0; j < 32; j += 2)
+    fma_f32x2(acc[j & 7], acc[(j & 7) + 1], w[j], w[j + 1], fmaxf(__uint_as_float(x[j]), 0.0f),
+              fmaxf(__uint_as_float(x[j + 1]), 0.0f));
 }
 __device__ __forceinline__ float head_reduce_finish(const float (&acc)[8]) {
   return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
