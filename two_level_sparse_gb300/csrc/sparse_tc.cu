@@ -16,18 +16,18 @@
 //               tcgen05.mma kind::mxf8f6f4 block_scale (M = 128 gathered
 //               positions, N = 64 heads, K = 32 each) into one of three
 //               accumulator stages;
-//   warps 1-3   gather: 16-byte cp.async copies of the tile's 16 candidate
-//               blocks (each 1 KB of contiguous K in its page) into a
-//               128-byte-swizzled MMA tile of a 9-deep ring, and their fp32
-//               scales into a separate 16-deep ring; completion is tracked by
-//               the barriers themselves (cp.async.mbarrier.arrive).  Several
-//               warps issue because one warp's copies in flight cap the rate;
+//   warps 1-3   gather a tile's 16 candidate blocks (each 1 KB of contiguous K
+//               in its page) into a 128-byte-swizzled MMA tile of a 9-deep
+//               ring: warp 1 with 8-row tensor-map loads for half of them,
+//               warps 2-3 with 16-byte cp.async for the other half (each path
+//               alone is capped well below what both reach together);
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
 //               then, two rows ahead, the page of every candidate block, the
 //               query widened from e2m1 to e4m3 and its scale factors staged;
-//   warps 8-15  two scoring warpgroups, tiles alternating: the same epilogue
-//               arithmetic as the dense pass, then one order-preserving key
-//               per candidate stored as one tensor-memory column per tile.
+//   warps 8-15  two scoring warpgroups, tiles alternating: each thread loads
+//               its position's K scale straight from the pool, then the same
+//               epilogue arithmetic as the dense pass and one order-preserving
+//               key per candidate stored as one tensor-memory column per tile.
 // Scores never leave the chip, and the shared memory they would need goes to
 // the gather ring instead.
 #include "ci_common.cuh"
@@ -38,7 +38,6 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kStages = 9;       // gathered K tiles in flight
-constexpr int kScaleSlots = 16;  // scale ring (released by the scoring warps)
 constexpr int kNumAcc = 3;
 constexpr int kSfaCol = 192;      // 4 columns of A scale factors (all 1.0)
 constexpr int kSfbCol = 196;      // two buffers of 4 columns of B scale factors
@@ -58,14 +57,12 @@ struct __align__(1024) Smem {
   uint8_t kv[kStages][kTileM * kDim];  // gathered A tiles (1024-aligned)
   uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered
   uint8_t sf[2][512];                  // query scale factors staged for tcgen05.cp
-  float ks[kScaleSlots][kTileM];       // K scales
   // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
   int32_t info[2][kMaxBlocks];
   uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
   int gbase[kMaxTiles], ebase[kMaxTiles];  // top-k: entries above / at the threshold before each tile
   int scan_part[2][kTopkThreads / 32];
   uint64_t k_full[kStages], tk_full[kStages], k_empty[kStages];
-  uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
   uint64_t t_full[kNumAcc], t_empty[kNumAcc];
   uint64_t q_full[2], q_empty[2];
   uint64_t info_full[2], info_empty[2];
@@ -398,10 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.tk_full[s], 1);                       // the tensor-map loads (transaction bytes)
       mbar_init(&sm.k_empty[s], 1);
     }
-    for (int s = 0; s < kScaleSlots; ++s) {
-      mbar_init(&sm.s_full[s], 32);
-      mbar_init(&sm.s_empty[s], 4);
-    }
     for (int s = 0; s < kNumAcc; ++s) {
       mbar_init(&sm.t_full[s], 1);
       mbar_init(&sm.t_empty[s], 4);
@@ -485,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // keeps in flight.  Both paths run side by side: warp 1 issues tensor-map
     // loads for the first kTmaBlocks blocks of a tile (one 8-row box each,
     // landing on its own swizzle atom), warps 2-3 copy the other blocks with
-    // 16-byte cp.async, and warp 2 also copies the K scales.
+    // 16-byte cp.async.
     const int gw = warp - kGatherWarp0;
     const uint32_t dst0 = sw128_offset(lane >> 3, (lane & 7) * 16), dst1 = sw128_offset(4 + (lane >> 3), (lane & 7) * 16);
-    Ring kr, sr;
+    Ring kr;
     int ri = 0;
     uint32_t issued = 0;  // warp 1: tiles whose tensor-map loads were issued
     bool ok = true;
@@ -498,8 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t) {
-        if ((gw == 1 && !warp_wait(&sm.s_empty[sr.idx], sr.phase ^ 1, abort_flag)) ||
-            !warp_wait(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
+        if (!warp_wait(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -519,16 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++issued;
         } else {
-          if (gw == 1) {  // scales: lane l copies half of block l / 2's eight fp32 scales
-            const int blk = lane >> 1, half = lane & 1;
-            const int slot = row_base + blk;
-            const int v = slot < r.nv ? info[slot] : -1;
-            if (v >= 0)
-              cp_async16(&sm.ks[sr.idx][blk * kBlock + half * 4],
-                         a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes + kPageValueBytes +
-                             (((v >> 4) & 7) * kBlock + half * 4) * 4);
-            cp_async_arrive_noinc(&sm.s_full[sr.idx]);
-          }
           // block blk: 1 KB contiguous in its page -> one 8-row swizzle atom;
           // lane l copies 16-byte chunks l and l + 32 (rows l / 8 and 4 + l / 8)
 #pragma unroll 2
@@ -545,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         }
         kr.next(kStages);
-        sr.next(kScaleSlots);
       }
       __syncwarp();
       if (ok) mbar_arrive(&sm.info_empty[b]);
@@ -613,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = (warp - kScoreWarp0) >> 2;  // scoring warpgroup 0 / 1
     const int quad = warp & 3;
     const int p = 32 * quad + lane;
-    Ring sr, ar;
+    Ring ar;
     uint32_t tseq = 0;
     int ri = 0;
     float w[kHeads];
@@ -644,6 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = t * kBlocksPerTile + (p >> 3);
           const int v = slot < r.nv ? sm.info[b][slot] : -1;
           const bool valid = v >= 0 && (p & 7) < (v & 15);
+          // this position's K scale, fetched now and used after the head sum
+          float kscale = 0.0f;
+          if (valid)
+            kscale = __ldg(reinterpret_cast<const float*>(a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes +
+                                                          kPageValueBytes) +
+                           ((v >> 4) & 7) * kBlock + (p & 7));
           if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
             ok = false;
             break;
@@ -662,17 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.t_empty[ar.idx]);
           const float score = head_reduce_finish(acc);
-          if (!warp_wait(&sm.s_full[sr.idx], sr.phase, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const float kscale = sm.ks[sr.idx][p];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.s_empty[sr.idx]);
           tmem_st1(score_col + t, valid ? order_key(score * kscale) : 0u);
           nvalid_seen += __popc(__ballot_sync(0xffffffffu, valid));
         }
-        sr.next(kScaleSlots);
         ar.next(kNumAcc);
       }
       if (!ok) break;
