@@ -68,31 +68,51 @@ __device__ __forceinline__ bool warp_wait_fast(uint64_t* bar, uint32_t parity, v
   return warp_wait(bar, parity, abort);
 }
 
-// Two IEEE round-to-nearest fused multiply-adds in one packed instruction
-// (a_i = w_i * r_i + a_i for i = 0, 1; the same results as two fmaf calls).
-__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float w0, float w1, float r0, float r1) {
-  asm("{\n\t.reg .b64 a, b, c;\n\t"
-      "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
-      "fma.rn.f32x2 a, b, c, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(w0), "f"(w1), "f"(r0), "f"(r1));
-}
-
 // ---------------------------------------------------------------- score epilogue
 // Head-weighted ReLU reduction of one (row, position) pair from its 64 fp32
 // accumulator columns, delivered in two halves of 32: eight partial sums
 // (head h feeds partial h % 8), combined in a fixed tree.  Every kernel that
-// scores a position uses this function, so identical K vectors give
-// bit-identical scores wherever they are scored.  Pairs of heads go through
-// one packed FMA (adjacent partial sums).
-__device__ __forceinline__ void head_reduce_half(float (&acc)[8], const uint32_t (&x)[32], const float* w) {
-#pragma unroll
-  for (int j = 0; j < 32; j += 2)
-    fma_f32x2(acc[j & 7], acc[(j & 7) + 1], w[j], w[j + 1], fmaxf(__uint_as_float(x[j]), 0.0f),
-              fmaxf(__uint_as_float(x[j + 1]), 0.0f));
+// scores a position uses these functions, so identical K vectors give
+// bit-identical scores wherever they are scored.
+//
+// The partial sums live as four packed pairs (2m, 2m + 1) and the head
+// weights as 32 packed pairs (w[2m], w[2m + 1]), low word first; heads 2m and
+// 2m + 1 go through two ReLUs and one fma.rn.f32x2 (two IEEE round-to-nearest
+// FMAs, the same results as two fmaf calls) without leaving the pair registers.
+struct HeadAcc {
+  unsigned long long p[4];
+};
+__device__ __forceinline__ void relu_fma_pair(unsigned long long& acc, unsigned long long w2, uint32_t x0,
+                                              uint32_t x1) {
+  asm("{\n\t.reg .f32 r0, r1;\n\t.reg .b64 c;\n\t"
+      "max.f32 r0, %2, 0f00000000;\n\tmax.f32 r1, %3, 0f00000000;\n\t"
+      "mov.b64 c, {r0, r1};\n\tfma.rn.f32x2 %0, %1, c, %0;\n\t}"
+      : "+l"(acc)
+      : "l"(w2), "r"(x0), "r"(x1));
 }
-__device__ __forceinline__ float head_reduce_finish(const float (&acc)[8]) {
-  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+// x: heads 32 half .. 32 half + 31 of the position; w2: their 16 weight pairs.
+__device__ __forceinline__ void head_reduce_half(HeadAcc& acc, const uint32_t (&x)[32], const unsigned long long* w2) {
+#pragma unroll
+  for (int m = 0; m < 16; ++m) relu_fma_pair(acc.p[m & 3], w2[m], x[2 * m], x[2 * m + 1]);
+}
+__device__ __forceinline__ float head_reduce_finish(const HeadAcc& acc) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[2 * i] = __uint_as_float(static_cast<uint32_t>(acc.p[i]));
+    a[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(acc.p[i] >> 32));
+  }
+  return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+// The 64 head weights of a row (16-byte aligned) as 32 packed pairs.
+__device__ __forceinline__ void load_head_weights(unsigned long long (&w2)[32], const float* w) {
+  const ulonglong2* wp = reinterpret_cast<const ulonglong2*>(w);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const ulonglong2 v = wp[j];
+    w2[2 * j] = v.x;
+    w2[2 * j + 1] = v.y;
+  }
 }
 
 // ---------------------------------------------------------------- page ids of K tiles

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t issued = 0;  // TMA thread: tiles whose loads were issued
   const int epi = warp >= kEpiWarp0 ? (warp - kEpiWarp0) >> 2 : -1;  // epilogue warpgroup
   const int quad = warp & 3;
-  float w[kHeads];
+  unsigned long long w2[32];  // head weights, packed pairs
 
   while (remaining > 0 && g < num_groups) {
     const int glen = group_len<R>(a, g);
@@ -228,15 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       row = R == 3 ? g * 3 + epi : g;
       if (row < a.p.rows) {
         rlen = max(scored_len(a, row), 0);  // 0 when the row is skipped: nothing is stored
-        const float4* wp = reinterpret_cast<const float4*>(a.p.w + static_cast<int64_t>(row) * kHeads);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float4 v = wp[j];
-          w[4 * j] = v.x;
-          w[4 * j + 1] = v.y;
-          w[4 * j + 2] = v.z;
-          w[4 * j + 3] = v.w;
-        }
+        load_head_weights(w2, a.p.w + static_cast<int64_t>(row) * kHeads);
       }
     }
     tc_fence_before();
@@ -325,15 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        HeadAcc part = {{0, 0, 0, 0}};
         uint32_t x[32];
         const uint32_t taddr = tmem_addr(tbase, 32 * quad, ai * N + col0);
         tmem_ld32(taddr, x);
         tmem_ld_wait();
-        head_reduce_half(part, x, w);
+        head_reduce_half(part, x, w2);
         tmem_ld32(taddr + 32, x);
         tmem_ld_wait();
-        head_reduce_half(part, x, w + 32);
+        head_reduce_half(part, x, w2 + 16);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.t_empty[ai]);

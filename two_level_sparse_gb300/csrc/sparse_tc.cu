@@ -597,20 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring ar;
     uint32_t tseq = 0;
     int ri = 0;
-    float w[kHeads];
+    unsigned long long w2[32];  // head weights, packed pairs
     bool ok = true;
     for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
       const RowInfo r = row_info(a, row, false);
       const int b = ri & 1;
-      const float4* wp = reinterpret_cast<const float4*>(a.p.w + static_cast<int64_t>(row) * kHeads);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 v = wp[j];
-        w[4 * j] = v.x;
-        w[4 * j + 1] = v.y;
-        w[4 * j + 2] = v.z;
-        w[4 * j + 3] = v.w;
-      }
+      load_head_weights(w2, a.p.w + static_cast<int64_t>(row) * kHeads);
       // the candidate page lookups (prepared with the row) tell which positions are live
       if (!warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag) ||
           (ri >= 2 && !warp_wait(&sm.sc_empty[b], ((ri >> 1) & 1) ^ 1, abort_flag))) {
@@ -636,15 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          HeadAcc acc = {{0, 0, 0, 0}};
           uint32_t x[32];
           const uint32_t taddr = tmem_addr(tbase, 32 * quad, ar.idx * kHeads);
           tmem_ld32(taddr, x);
           tmem_ld_wait();
-          head_reduce_half(acc, x, w);
+          head_reduce_half(acc, x, w2);
           tmem_ld32(taddr + 32, x);
           tmem_ld_wait();
-          head_reduce_half(acc, x, w + 32);
+          head_reduce_half(acc, x, w2 + 16);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.t_empty[ar.idx]);
