@@ -18,8 +18,8 @@
 //               accumulator stages;
 //   warps 1-3   gather a tile's 16 candidate blocks (each 1 KB of contiguous K
 //               in its page) into a 128-byte-swizzled MMA tile of a 9-deep
-//               ring: warp 1 with 8-row tensor-map loads for half of them,
-//               warps 2-3 with 16-byte cp.async for the other half (each path
+//               ring: warp 1 with 8-row tensor-map loads for 6 of them,
+//               warps 2-3 with 16-byte cp.async for the other 10 (each path
 //               alone is capped well below what both reach together);
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
 //               then, two rows ahead, the page of every candidate block, the
@@ -46,7 +46,7 @@ constexpr int kBlocksPerTile = kTileM / kBlock;  // 16
 constexpr int kMaxBlocks = 2176;                 // >= topk + 1 for every supported topk
 constexpr int kMaxTiles = kMaxBlocks / kBlocksPerTile;  // 136
 constexpr int kGatherWarp0 = 1, kGatherWarps = 3;  // warp 1 tensor-map loads, warps 2-3 cp.async
-constexpr int kTmaBlocks = 8;  // blocks of a tile fetched by tensor-map loads (the rest by cp.async)
+constexpr int kTmaBlocks = 6;  // blocks of a tile fetched by tensor-map loads (the rest by cp.async)
 constexpr int kTopkWarp0 = 4, kTopkThreads = 128, kTopkBar = 2;  // also the next-row prep
 constexpr int kPrepThreads = kTopkThreads;
 constexpr int kScoreWarp0 = 8;
@@ -59,6 +59,7 @@ struct __align__(1024) Smem {
   uint8_t sf[2][512];                  // query scale factors staged for tcgen05.cp
   // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
   int32_t info[2][kMaxBlocks];
+  int32_t bid[2][kMaxBlocks];  // the candidate block ids, for the top-k's output positions
   uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
   int gbase[kMaxTiles], ebase[kMaxTiles];  // top-k: entries above / at the threshold before each tile
   int scan_part[2][kTopkThreads / 32];
@@ -166,6 +167,7 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
       else
         v = (pid[j] << 7) | ((blk[j] & 7) << 4) | min(kBlock, r.L - blk[j] * kBlock);
       sm.info[b][i] = v;
+      sm.bid[b][i] = blk[j];
     }
   }
   mbar_arrive(&sm.info_full[b]);
@@ -566,13 +568,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int k = min(a.topk, sm.vcount[b]);
-      const int32_t* brow = a.blocks + static_cast<int64_t>(row) * a.blocks_stride;
       int32_t* out = a.out_pos + static_cast<int64_t>(row) * a.out_stride;
       float* osc = a.out_score != nullptr ? a.out_score + static_cast<int64_t>(row) * a.out_stride : nullptr;
       if (k > 0) {
         tmem_topk(sm, lane_base + kScoreCol + b * kMaxTiles, r.ntiles, k, kt,
                   [&](int rank, int t, int p, uint32_t u) {
-                    out[rank] = brow[t * kBlocksPerTile + (p >> 3)] * kBlock + (p & 7);
+                    out[rank] = sm.bid[b][t * kBlocksPerTile + (p >> 3)] * kBlock + (p & 7);
                     if (osc) osc[rank] = order_key_inv(u);
                   });
       }
