@@ -441,8 +441,8 @@ def select_traffic():
 
 
 def head_launches(steps, world):
-    # per step: dense 1 + publish 2 (K and P + 1) + select 5
-    return steps * 8
+    # per step: dense 1 + publish 1 (K and P + 1 together) + select 5
+    return steps * 7
 
 
 if __name__ == "__main__":

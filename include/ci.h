@@ -14,6 +14,9 @@
  *                            row's newest block forced to +inf;
  *     ci_publish_blocks      each row's top topk_blocks block ids by key,
  *                            ascending, INT32_MAX padded;
+ *     ci_publish_blocks2     the same for two block counts at once (the
+ *                            consumers' K and the source's own P + 1),
+ *                            reading the keys once;
  *   level two, once per layer (the source itself and each consumer):
  *     ci_select_sparse       scores only the positions inside a row's
  *                            published blocks and returns its top-k positions,
@@ -135,6 +138,22 @@ CI_API int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const
 CI_API int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys,
                       int64_t keys_stride, int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride,
                       int32_t* nvalid, int32_t* dev_err, void* stream);
+
+/*
+ * Two selections from the same keys in one pass: exactly the results of
+ * ci_publish_blocks(..., topk_blocks, blocks, blocks_stride, nvalid, ...) and
+ * ci_publish_blocks(..., topk_blocks2, blocks2, blocks2_stride, nvalid2, ...),
+ * with each row's keys read once.  The step of the two-level method needs
+ * both: the consumers select within the top K blocks, the source within its
+ * top P + 1 (sglang PR #40352, Design, "Level one").  blocks2 == NULL makes it
+ * ci_publish_blocks (topk_blocks2, blocks2_stride and nvalid2 are then
+ * ignored); otherwise nvalid2 must not be NULL, 1 <= topk_blocks2 <= 16384 and
+ * blocks2_stride >= topk_blocks2.  Same errors as ci_publish_blocks.
+ */
+CI_API int ci_publish_blocks2(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys,
+                       int64_t keys_stride, int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride,
+                       int32_t* nvalid, int32_t topk_blocks2, int32_t* blocks2, int64_t blocks2_stride,
+                       int32_t* nvalid2, int32_t* dev_err, void* stream);
 
 /*
  * Level two: a layer's top-k positions inside the candidate blocks.

@@ -29,7 +29,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(
-        ["ci_publish_blocks", "ci_score_dense_amax8", "ci_select_sparse", "ci_strerror", "ci_version"])
+        ["ci_publish_blocks", "ci_publish_blocks2", "ci_score_dense_amax8", "ci_select_sparse", "ci_strerror",
+         "ci_version"])
 
 
 def test_library_exports_every_declared_symbol(ci):
@@ -81,6 +82,15 @@ def test_publish_host_checks(ci):
     assert f(P, 2, 64, N, 8, 16, P, 16, P, N, N) == -1
     assert f(P, 2, 400000, P, 50000, 16, P, 16, P, N, N) == -4  # longer than supported
     assert f(P, 2, 64, ctypes.c_void_p(0x1004), 8, 16, P, 16, P, N, N) == -3
+
+
+def test_publish_pair_host_checks(ci):
+    f = ci.lib.ci_publish_blocks2
+    assert f(N, 0, 0, N, 8, 16, N, 16, N, 4, N, 4, N, N, N) == 0
+    assert f(P, 2, 64, P, 8, 16, P, 16, P, 0, P, 16, P, N, N) == -4  # topk_blocks2 < 1
+    assert f(P, 2, 64, P, 8, 16, P, 16, P, 20, P, 16, P, N, N) == -2  # blocks2 stride < topk_blocks2
+    assert f(P, 2, 64, P, 8, 16, P, 16, P, 4, P, 4, N, N, N) == -1  # nvalid2 missing
+    assert f(P, 2, 64, P, 8, 0, P, 16, P, 4, N, 4, N, N, N) == -4  # first selection checked as before
 
 
 def test_select_host_checks(ci):

@@ -200,3 +200,45 @@ def subset_workload(wl_dev, rows):
     pt = wl_dev.page_table[idx].cpu() if wl_dev.layout == synth.LAYOUT_DECODE else wl_dev.page_table.cpu()
     return synth.Workload(wl_dev.name, wl_dev.layout, wl_dev.seq_len[idx].cpu(), pt, layers, wl_dev.topk_blocks,
                           wl_dev.topk)
+
+
+@needs_cuda
+@pytest.mark.parametrize("K1,K2", [(2048, 513), (128, 513), (513, 64)])
+def test_publish_pair_equals_two_single_publishes(ci, K1, K2):
+    """ci_publish_blocks2 returns exactly the two single selections, which
+    equal the oracle's block selection (ties toward the lower block id)."""
+    g = torch.Generator().manual_seed(7)
+    rows = 40
+    lens = torch.randint(1, 40000, (rows,), generator=g, dtype=torch.int32)
+    lens[:4] = torch.tensor([1, 8 * K1, 8 * K2 + 3, 8 * max(K1, K2) + 1], dtype=torch.int32)
+    max_len = int(lens.max())
+    stride = ((max_len + 7) // 8 + 7) // 8 * 8
+    # few distinct values so that many keys tie
+    keys = (torch.randint(0, 300, (rows, stride), generator=g).float() / 7.0 - 20.0)
+    keys[5, :200] = -float("inf")
+    dev = "cuda"
+    kd, ld = keys.to(dev), lens.to(dev)
+    b1 = torch.empty(rows, K1, dtype=torch.int32, device=dev)
+    n1 = torch.empty(rows, dtype=torch.int32, device=dev)
+    b2 = torch.empty(rows, K2, dtype=torch.int32, device=dev)
+    n2 = torch.empty(rows, dtype=torch.int32, device=dev)
+    s1, m1 = torch.empty_like(b1), torch.empty_like(n1)
+    s2, m2 = torch.empty_like(b2), torch.empty_like(n2)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ci.ci_publish_blocks2(ld, max_len, kd, K1, b1, n1, K2, b2, n2, dev_err=err)
+    ci.ci_publish_blocks(ld, max_len, kd, K1, s1, m1, dev_err=err)
+    ci.ci_publish_blocks(ld, max_len, kd, K2, s2, m2, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(b1, s1) and torch.equal(n1, m1)
+    assert torch.equal(b2, s2) and torch.equal(n2, m2)
+    b1h, b2h = b1.cpu().numpy(), b2.cpu().numpy()
+    for t in range(rows):
+        nb = O.num_blocks(int(lens[t]))
+        kr = keys[t, :nb].double().numpy()
+        for K, out in ((K1, b1h), (K2, b2h)):
+            ids, nv = O.select_blocks(kr, nb, K)
+            assert nv == min(nb, K)
+            assert np.array_equal(out[t, :nv], ids[:nv]), (t, K)
+            assert np.all(out[t, nv:] == 0x7FFFFFFF)
+

@@ -34,6 +34,7 @@ _I64 = ctypes.c_int64
 SIGNATURES = {
     "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
     "ci_publish_blocks": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P, _P],
+    "ci_publish_blocks2": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _P],
     "ci_select_sparse": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _I32, _I32, _P, _I64, _P, _I32, _I32, _P, _P,
                          _I64, _P, _P],
     "ci_strerror": [ctypes.c_int],
@@ -119,6 +120,20 @@ def ci_publish_blocks(seq_len, max_len, keys, topk_blocks, blocks, nvalid, dev_e
     _check("ci_publish_blocks", lib.ci_publish_blocks(
         _ptr(seq_len), rows, int(max_len), _ptr(keys), int(keys.stride(0)), int(topk_blocks), _ptr(blocks),
         int(blocks.stride(0)), _ptr(nvalid), _ptr(dev_err), _stream(stream)))
+
+
+def ci_publish_blocks2(seq_len, max_len, keys, topk_blocks, blocks, nvalid, topk_blocks2, blocks2, nvalid2,
+                       dev_err=None, stream=None):
+    """Two block counts from the same keys in one pass (see include/ci.h)."""
+    _expect(seq_len, torch.int32, "seq_len")
+    _expect(keys, torch.float32, "keys")
+    for t, n in ((blocks, "blocks"), (nvalid, "nvalid"), (blocks2, "blocks2"), (nvalid2, "nvalid2")):
+        _expect(t, torch.int32, n)
+    rows = int(seq_len.shape[0])
+    _check("ci_publish_blocks2", lib.ci_publish_blocks2(
+        _ptr(seq_len), rows, int(max_len), _ptr(keys), int(keys.stride(0)), int(topk_blocks), _ptr(blocks),
+        int(blocks.stride(0)), _ptr(nvalid), int(topk_blocks2), _ptr(blocks2), int(blocks2.stride(0)), _ptr(nvalid2),
+        _ptr(dev_err), _stream(stream)))
 
 
 def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, blocks, nvalid, max_blocks, topk,

@@ -111,19 +111,32 @@ int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float*
   return launched(ci::launch_dense_amax8(a, static_cast<cudaStream_t>(stream)));
 }
 
-int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys, int64_t keys_stride,
-                      int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride, int32_t* nvalid, int32_t* dev_err,
-                      void* stream) {
+int ci_publish_blocks2(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys, int64_t keys_stride,
+                       int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride, int32_t* nvalid,
+                       int32_t topk_blocks2, int32_t* blocks2, int64_t blocks2_stride, int32_t* nvalid2,
+                       int32_t* dev_err, void* stream) {
   if (rows < 0 || max_len < 0) return CI_ERR_SHAPE;
   if (topk_blocks < 1 || topk_blocks > 16384) return CI_ERR_RANGE;
+  if (blocks2 != nullptr && (topk_blocks2 < 1 || topk_blocks2 > 16384)) return CI_ERR_RANGE;
   if (max_len > 393216) return CI_ERR_RANGE;
   if (rows == 0) return CI_OK;
   if (!seq_len || !keys || !blocks || !nvalid) return CI_ERR_NULL;
+  if (blocks2 != nullptr && !nvalid2) return CI_ERR_NULL;
   if (blocks_stride < topk_blocks) return CI_ERR_SHAPE;
+  if (blocks2 != nullptr && blocks2_stride < topk_blocks2) return CI_ERR_SHAPE;
   if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
   if (!aligned(keys, 16)) return CI_ERR_ALIGN;
-  ci::PublishArgs a{seq_len, rows, max_len, keys, keys_stride, topk_blocks, blocks, blocks_stride, nvalid, dev_err};
+  ci::PublishArgs a{seq_len, rows,   max_len, keys, keys_stride, topk_blocks,
+                    blocks,  blocks_stride, nvalid, blocks2 ? topk_blocks2 : 0, blocks2, blocks2_stride,
+                    nvalid2, dev_err};
   return launched(ci::launch_publish(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys, int64_t keys_stride,
+                      int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride, int32_t* nvalid, int32_t* dev_err,
+                      void* stream) {
+  return ci_publish_blocks2(seq_len, rows, max_len, keys, keys_stride, topk_blocks, blocks, blocks_stride, nvalid, 0,
+                            nullptr, 0, nullptr, dev_err, stream);
 }
 
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,

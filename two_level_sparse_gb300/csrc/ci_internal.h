@@ -38,6 +38,10 @@ struct PublishArgs {
   int32_t* blocks;
   int64_t blocks_stride;
   int32_t* nvalid;
+  int32_t topk_blocks2;  // second selection from the same keys (0: none)
+  int32_t* blocks2;
+  int64_t blocks2_stride;
+  int32_t* nvalid2;
   int32_t* dev_err;
 };
 

@@ -6,8 +6,8 @@ publishes its candidate blocks and runs its own top-512; each consumer selects
 within the published blocks):
 
   ci_score_dense_amax8(source)                   keys, rows with > min(K, P+1) blocks
-  ci_publish_blocks(keys, K)                     the consumers' candidates
-  ci_publish_blocks(keys, P + 1)  (if P+1 != K)  the source's own candidates
+  ci_publish_blocks2(keys, K, P + 1)             the consumers' and the source's candidates
+                                                 (ci_publish_blocks when P + 1 == K)
   ci_select_sparse(source, P + 1 blocks)         the source's top-P
   ci_select_sparse(consumer j, K blocks)         each consumer's top-P
 
@@ -54,7 +54,7 @@ class IndexerStep:
 
     def launches(self) -> int:
         """Kernels one run() enqueues."""
-        return 1 + (1 if self.Kp == self.K else 2) + len(self.wl.layers)
+        return 2 + len(self.wl.layers)
 
     def run(self, stream=None, skip_dense=False, mark=None):
         """Enqueue the step on `stream` (default: torch's current stream).
@@ -70,13 +70,13 @@ class IndexerStep:
             ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, skip_le_blocks=self.skip, keys=self.keys,
                                     **common)
             mark("dense")
-        ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
-                             dev_err=self.dev_err, stream=stream)
-        mark("publish")
         if self.Kp != self.K:
-            ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.Kp, self.blocks_src, self.nvalid_src,
+            ci.ci_publish_blocks2(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid, self.Kp,
+                                  self.blocks_src, self.nvalid_src, dev_err=self.dev_err, stream=stream)
+        else:
+            ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
                                  dev_err=self.dev_err, stream=stream)
-            mark("publish")
+        mark("publish")
         for j, layer in enumerate(wl.layers):
             blocks, nvalid, mb = (self.blocks_src, self.nvalid_src, self.Kp) if j == 0 else (self.blocks,
                                                                                             self.nvalid, self.K)
