@@ -153,14 +153,26 @@ __global__ void __launch_bounds__(kThreads, 1) publish_kernel(const PublishArgs 
   __syncthreads();
   const float* keys = a.keys + static_cast<int64_t>(row) * a.keys_stride;
   const int nb4 = nb & ~3;
-  for (int i = tid * 4; i < nb4; i += kThreads * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(keys + i);
-    const uint4 u = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
-    *reinterpret_cast<uint4*>(sk + i) = u;
-    atomicAdd(&sh.h1[u.x >> 20], 1u);
-    atomicAdd(&sh.h1[u.y >> 20], 1u);
-    atomicAdd(&sh.h1[u.z >> 20], 1u);
-    atomicAdd(&sh.h1[u.w >> 20], 1u);
+  // kBatch 16-byte loads in flight per thread before their codes are counted
+  constexpr int kBatch = 8;
+  for (int i0 = tid * 4; i0 < nb4; i0 += kThreads * 4 * kBatch) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kThreads * 4;
+      v[j] = i < nb4 ? *reinterpret_cast<const float4*>(keys + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kThreads * 4;
+      if (i >= nb4) break;
+      const uint4 u = make_uint4(order_key(v[j].x), order_key(v[j].y), order_key(v[j].z), order_key(v[j].w));
+      *reinterpret_cast<uint4*>(sk + i) = u;
+      atomicAdd(&sh.h1[u.x >> 20], 1u);
+      atomicAdd(&sh.h1[u.y >> 20], 1u);
+      atomicAdd(&sh.h1[u.z >> 20], 1u);
+      atomicAdd(&sh.h1[u.w >> 20], 1u);
+    }
   }
   for (int i = nb4 + tid; i < nb; i += kThreads) {
     const uint32_t u = order_key(keys[i]);
