@@ -87,6 +87,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int N = 64 * R;                    // MMA N
   constexpr int kNumAcc = R == 3 ? 2 : 4;      // accumulator stages (power of two)
   constexpr int kEpiPerTile = R == 3 ? 3 : 1;  // epilogue warpgroups consuming each tile
+  // With R = 3 every epilogue warp reads every tile's K scales in order, and
+  // the copy into scale slot u + 16 waits for MMA u + 8, which needs all of
+  // them past tile u + 6: the slot is free without a barrier of its own.
+  // Round-robin warpgroups (R = 1) give no such order, so they release slots.
+  constexpr bool kScaleRelease = R != 3;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
           const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
           if (!warp_wait_fast(&sm.k_empty[ki], kp ^ 1, abort_flag) ||
-              !warp_wait_fast(&sm.s_empty[si], sp ^ 1, abort_flag)) {
+              (kScaleRelease && !warp_wait_fast(&sm.s_empty[si], sp ^ 1, abort_flag))) {
             if (lane == 0) set_abort(sm, a.p.dev_err);
             ok = false;
             break;
@@ -335,8 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const float kscale = sm.ks[si][p];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_empty[si]);
+        if (kScaleRelease) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.s_empty[si]);
+        }
         const int pos = t * kTileM + p;
         float v = pos < rlen ? score * kscale : -__int_as_float(0x7f800000);
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
