@@ -242,3 +242,21 @@ def test_publish_pair_equals_two_single_publishes(ci, K1, K2):
             assert np.array_equal(out[t, :nv], ids[:nv]), (t, K)
             assert np.all(out[t, nv:] == 0x7FFFFFFF)
 
+
+
+@needs_cuda
+@pytest.mark.parametrize("cid", [1, 3])
+def test_positions_without_scores_match_with_scores(ci, cid):
+    """The benchmark runs the step without the optional score output; its
+    positions must be exactly those of the scored run the oracle checks."""
+    from two_level_sparse_gb300.step import IndexerStep
+
+    dev = synth.config_workload(cid, device="cuda")
+    a = IndexerStep(dev, with_scores=True)
+    b = IndexerStep(dev, with_scores=False)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert int(a.dev_err.item()) == 0 and int(b.dev_err.item()) == 0
+    assert torch.equal(a.pos, b.pos)
+    assert torch.equal(a.blocks, b.blocks) and torch.equal(a.blocks_src, b.blocks_src)

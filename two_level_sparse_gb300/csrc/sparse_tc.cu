@@ -177,8 +177,9 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
 // Top-k of one row whose order keys sit in tensor memory: column t of the
 // buffer holds tile t, lane p the tile's position p (key 0 = no candidate).
 // Run by the 128 threads of warps 4-7, thread kt owning lane kt.
-template <class Emit>
-__device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, int k, int kt, Emit emit) {
+template <class EmitPos, class EmitScore>
+__device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, int k, int kt, EmitPos emit_pos,
+                                          bool want_scores, EmitScore emit_score) {
   TopkShared& sh = sm.topk;
   const int q = kt >> 5, l = kt & 31;
   uint32_t x[32];
@@ -351,9 +352,30 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
     }
   }
   named_sync(kTopkBar, kTopkThreads);
-  // Emit: only the tiles where this lane holds a selected entry cost more than
-  // two compares.  Rank = entries above the threshold before it + entries at
-  // the threshold before it (capped at need_eq), in (tile, position) order.
+  // Positions, tile-parallel: thread kt walks the selected entries of tiles
+  // kt and kt + 128 (about P / tiles each) in position order.  Rank = entries
+  // above the threshold before it + entries at it before it (capped at
+  // need_eq), in (tile, position) order.
+  for (int t = kt; t < nt; t += kTopkThreads) {
+    const uint4 g4 = sm.mgt[t], e4 = sm.meq[t];
+    const uint32_t g[4] = {g4.x, g4.y, g4.z, g4.w}, e[4] = {e4.x, e4.y, e4.z, e4.w};
+    uint32_t gtb = static_cast<uint32_t>(sm.gbase[t]), eqb = static_cast<uint32_t>(sm.ebase[t]);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t bits = g[w] | e[w];
+      while (bits) {
+        const int lb = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const uint32_t below = (1u << lb) - 1u;
+        const uint32_t gt_before = gtb + __popc(g[w] & below), eq_before = eqb + __popc(e[w] & below);
+        if (((g[w] >> lb) & 1u) || eq_before < need_eq) emit_pos(static_cast<int>(gt_before + min(eq_before, need_eq)), t, 32 * w + lb);
+      }
+      gtb += __popc(g[w]);
+      eqb += __popc(e[w]);
+    }
+  }
+  if (!want_scores) return;
+  // Scores, lane-parallel (only this lane can read its keys): the same ranks.
   const uint32_t lt = lanemask_lt();
   for (int c0 = 0; c0 < nt; c0 += 32) {
     tmem_ld32(lane_col0 + c0, x);
@@ -375,7 +397,7 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
           gtb += __popc(g[w]);
           eqb += __popc(e[w]);
         }
-      if (is_gt || eqb < need_eq) emit(static_cast<int>(gtb + min(eqb, need_eq)), t, kt, x[j]);
+      if (is_gt || eqb < need_eq) emit_score(static_cast<int>(gtb + min(eqb, need_eq)), x[j]);
     }
   }
 }
@@ -571,11 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t* out = a.out_pos + static_cast<int64_t>(row) * a.out_stride;
       float* osc = a.out_score != nullptr ? a.out_score + static_cast<int64_t>(row) * a.out_stride : nullptr;
       if (k > 0) {
-        tmem_topk(sm, lane_base + kScoreCol + b * kMaxTiles, r.ntiles, k, kt,
-                  [&](int rank, int t, int p, uint32_t u) {
-                    out[rank] = sm.bid[b][t * kBlocksPerTile + (p >> 3)] * kBlock + (p & 7);
-                    if (osc) osc[rank] = order_key_inv(u);
-                  });
+        tmem_topk(
+            sm, lane_base + kScoreCol + b * kMaxTiles, r.ntiles, k, kt,
+            [&](int rank, int t, int p) { out[rank] = sm.bid[b][t * kBlocksPerTile + (p >> 3)] * kBlock + (p & 7); },
+            osc != nullptr, [&](int rank, uint32_t u) { osc[rank] = order_key_inv(u); });
       }
       for (int i = max(k, 0) + kt; i < a.topk; i += kTopkThreads) {
         out[i] = -1;
