@@ -167,114 +167,4 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// ---------------------------------------------------------------- block top-k
-struct TopkShared {
-  uint32_t hist[256];
-  uint32_t warp_gt[32];
-  uint32_t warp_eq[32];
-  uint32_t sel_digit, sel_remaining, sel_match;
-};
-
-// Selects the k largest of the uint32 keys sk[0..n) (k <= n), ties toward the
-// lower index, and calls emit(rank, index, key) once per selected entry with
-// rank = its place in ascending index order.  Radix select on 8-bit digits
-// from the top, stopping as soon as the threshold digit's bucket is taken
-// whole, then an ordered compaction.  Executed by `nthreads` threads (a
-// multiple of 32, thread ids 0..nthreads-1) that sync on named barrier bar_id.
-template <class Emit>
-__device__ __forceinline__ void block_topk(const uint32_t* sk, int n, int k, TopkShared& sh, int tid, int nthreads,
-                                           int bar_id, Emit emit) {
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += nthreads) sh.hist[i] = 0;
-    named_sync(bar_id, nthreads);
-    for (int i = tid; i < n; i += nthreads) {
-      const uint32_t u = sk[i];
-      if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & 255u], 1u);
-    }
-    named_sync(bar_id, nthreads);
-    if (tid < 32) {
-      uint32_t c[8], lane_sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = sh.hist[tid * 8 + j];
-        lane_sum += c[j];
-      }
-      uint32_t suffix = lane_sum;  // sum over lanes >= tid
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xffffffffu, suffix, off);
-        if (tid + off < 32) suffix += v;
-      }
-      const uint32_t above = suffix - lane_sum;  // keys whose digit lies above this lane's bins
-      if (above < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= suffix) {
-        uint32_t acc = above;
-#pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
-            sh.sel_digit = tid * 8 + j;
-            sh.sel_remaining = remaining - acc;
-            sh.sel_match = c[j];
-            break;
-          }
-          acc += c[j];
-        }
-      }
-    }
-    named_sync(bar_id, nthreads);
-    const uint32_t d = sh.sel_digit;
-    remaining = static_cast<int>(sh.sel_remaining);
-    const uint32_t match = sh.sel_match;
-    prefix |= d << shift;
-    mask |= 0xFFu << shift;
-    if (match == static_cast<uint32_t>(remaining)) break;  // the whole bucket is taken
-  }
-  const int need_eq = remaining;
-  // ordered compaction: warps own contiguous segments
-  const int nwarps = nthreads >> 5, wid = tid >> 5, lane = tid & 31;
-  const int seg = ((n + nwarps - 1) / nwarps + 31) & ~31;
-  const int begin = min(n, wid * seg), end = min(n, begin + seg);
-  uint32_t gt = 0, eq = 0;
-  for (int i = begin + lane; i < end; i += 32) {
-    const uint32_t m = sk[i] & mask;
-    gt += m > prefix;
-    eq += m == prefix;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, off);
-    eq += __shfl_xor_sync(0xffffffffu, eq, off);
-  }
-  if (lane == 0) {
-    sh.warp_gt[wid] = gt;
-    sh.warp_eq[wid] = eq;
-  }
-  named_sync(bar_id, nthreads);
-  uint32_t gt_before = 0, eq_before = 0;
-  for (int w = 0; w < wid; ++w) {
-    gt_before += sh.warp_gt[w];
-    eq_before += sh.warp_eq[w];
-  }
-  const uint32_t lt = lanemask_lt();
-  for (int base = begin; base < end; base += 32) {
-    const int i = base + lane;
-    const bool valid = i < end;
-    const uint32_t u = valid ? sk[i] : 0u;
-    const uint32_t m = u & mask;
-    const bool is_gt = valid && m > prefix;
-    const bool is_eq = valid && m == prefix;
-    const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
-    const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
-    const uint32_t eq_rank = eq_before + __popc(be & lt);
-    if (is_gt || (is_eq && eq_rank < static_cast<uint32_t>(need_eq))) {
-      const uint32_t rank = gt_before + __popc(bg & lt) + min(eq_rank, static_cast<uint32_t>(need_eq));
-      emit(static_cast<int>(rank), i, u);
-    }
-    gt_before += __popc(bg);
-    eq_before += __popc(be);
-  }
-  named_sync(bar_id, nthreads);  // sh is reused by the caller's next selection
-}
-
 }  // namespace ci

@@ -53,6 +53,14 @@ constexpr int kScoreWarp0 = 8;
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;
 static_assert(kScoreCol + 2 * kMaxTiles + 32 <= 512, "score columns must fit in tensor memory");
 
+// Top-k working set: radix digits of up to kDigitBits bits.
+constexpr int kDigitBits = 11;
+struct TopkShared {
+  uint32_t hist[1 << kDigitBits];
+  uint32_t part[kTopkThreads / 32];
+  uint32_t sel_digit, sel_remaining, sel_match;
+};
+
 struct __align__(1024) Smem {
   uint8_t kv[kStages][kTileM * kDim];  // gathered A tiles (1024-aligned)
   uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered
@@ -77,6 +85,7 @@ struct __align__(1024) Smem {
   uint32_t kmin, kmax;
   TopkShared topk;
 };
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
 
 __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
   sm.abort_flag = 1;
@@ -214,9 +223,10 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   uint32_t prefix = mn & mask;
   int remaining = k;
   while (hi > 0) {
-    const int width = min(8, hi), shift = hi - width;
+    const int width = min(kDigitBits, hi), shift = hi - width;
     const uint32_t dmask = (1u << width) - 1u;
-    for (int i = kt; i < 256; i += kTopkThreads) sh.hist[i] = 0;
+    const int nbins = 1 << width;
+    for (int i = kt; i < nbins; i += kTopkThreads) sh.hist[i] = 0;
     named_sync(kTopkBar, kTopkThreads);
     for (int c0 = 0; c0 < nt; c0 += 32) {
       tmem_ld32(lane_col0 + c0, x);
@@ -226,32 +236,39 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
         if (c0 + j < nt && (x[j] & mask) == prefix) atomicAdd(&sh.hist[(x[j] >> shift) & dmask], 1u);
     }
     named_sync(kTopkBar, kTopkThreads);
-    if (kt < 32) {
-      uint32_t c[8], lane_sum = 0;
+    // the threshold digit: thread kt owns bins [16 kt, 16 kt + 16)
+    constexpr int kPer = (1 << kDigitBits) / kTopkThreads;
+    uint32_t c[kPer], lsum = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = sh.hist[kt * 8 + j];
-        lane_sum += c[j];
-      }
-      uint32_t suffix = lane_sum;
+    for (int j = 0; j < kPer; ++j) {
+      const int bin = kt * kPer + j;
+      c[j] = bin < nbins ? sh.hist[bin] : 0u;
+      lsum += c[j];
+    }
+    uint32_t suffix = lsum;  // over lanes >= l
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xffffffffu, suffix, off);
-        if (kt + off < 32) suffix += v;
-      }
-      const uint32_t above = suffix - lane_sum;
-      if (above < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= suffix) {
-        uint32_t acc = above;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xffffffffu, suffix, o);
+      if (l + o < 32) suffix += v;
+    }
+    if (l == 0) sh.part[q] = suffix;
+    named_sync(kTopkBar, kTopkThreads);
+    uint32_t above = suffix - lsum;
 #pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
-            sh.sel_digit = kt * 8 + j;
-            sh.sel_remaining = remaining - acc;
-            sh.sel_match = c[j];
-            break;
-          }
-          acc += c[j];
+    for (int w = 0; w < kTopkThreads / 32; ++w)
+      if (w > q) above += sh.part[w];
+    const uint32_t want = static_cast<uint32_t>(remaining);
+    if (above < want && want <= above + lsum) {
+      uint32_t acc = above;
+#pragma unroll
+      for (int j = kPer - 1; j >= 0; --j) {
+        if (acc + c[j] >= want) {
+          sh.sel_digit = kt * kPer + j;
+          sh.sel_remaining = want - acc;
+          sh.sel_match = c[j];
+          break;
         }
+        acc += c[j];
       }
     }
     named_sync(kTopkBar, kTopkThreads);
