@@ -40,6 +40,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of `values` over all ranks (the slowest replica
+    sets the job's time); identity on one rank."""
+    values = [float(v) for v in values]
+    if world <= 1:
+        return values
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def emit_line(line, rank):
+    """Rank 0 alone prints the job's JSON line."""
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -260,7 +277,7 @@ def run_reference(args):
         "cpu_baseline": {"value": value, "unit": "ms", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit_line(line, rank)
     return 0
 
 
@@ -337,10 +354,8 @@ def main():
     ms_dense = statistics.mean(head["t_dense"])
     ms_select = statistics.mean(head["t_select"])
     ms_publish = statistics.mean(head["t_publish"])
-    if world > 1:
-        t = torch.tensor([ms_step, ms_dense, ms_select, ms_publish], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, ms_dense, ms_select, ms_publish = t.tolist()
+    ms_step, ms_dense, ms_select, ms_publish = max_over_ranks([ms_step, ms_dense, ms_select, ms_publish], world,
+                                                              "cuda")
     wl = head["wl"]
     err = int(head["step"].dev_err.item())
     flops, kbytes, positions = algorithmic_counts(wl)
@@ -351,10 +366,7 @@ def main():
     sel_gbs = sel_bytes / (ms_select * 1e-3) / 1e9
     e2e_ms, h2d, d2h = head.get("e2e", ([float("nan")], 0, 0))
     e2e_val = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_val], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_val = t.item()
+    (e2e_val,) = max_over_ranks([e2e_val], world, "cuda")
 
     secondary = []
     if not args.no_secondary:
@@ -411,8 +423,7 @@ def main():
             "value": cpu_ms, "unit": "ms", "cores": cpu_threads, "kind": "oracle",
             "sample": f"{cpu_rows} of {nrows} rows (last, first, middle), all 5 layers, extrapolated linearly"},
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    emit_line(line, rank)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
