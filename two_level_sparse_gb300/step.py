@@ -16,6 +16,10 @@ newest block's key is +inf and every other block that outranks a position's
 block holds a distinct higher-scoring position), so the source's top-P over
 its top-(P+1) blocks is its dense top-P, and the source gathers only those.
 
+With fewer rows than SMs a select launch leaves SMs idle, so the five selects
+(independent of one another) run side by side on streams forked from and
+joined back into the caller's stream.
+
 This module only allocates the output buffers (torch device memory) and
 marshals arguments; all computation runs in libci.so.
 """
@@ -51,6 +55,11 @@ class IndexerStep:
         self.pos = torch.empty(nl, self.rows, self.P, dtype=i32, device=dev)
         self.score = torch.empty(nl, self.rows, self.P, dtype=torch.float32, device=dev) if with_scores else None
         self.dev_err = torch.zeros(1, dtype=i32, device=dev)
+        # A select launch gives each of its CTAs (one per SM) whole rows; with
+        # fewer rows than SMs the layers' selects run side by side on their
+        # own streams (they share only read-only inputs).
+        self.concurrent = dev.type == "cuda" and self.rows < torch.cuda.get_device_properties(dev).multi_processor_count
+        self.side = [torch.cuda.Stream(device=dev) for _ in range(nl - 1)] if self.concurrent else []
 
     def launches(self) -> int:
         """Kernels one run() enqueues."""
@@ -77,12 +86,28 @@ class IndexerStep:
             ci.ci_publish_blocks(wl.seq_len, self.max_len, self.keys, self.K, self.blocks, self.nvalid,
                                  dev_err=self.dev_err, stream=stream)
         mark("publish")
+        main = stream if stream is not None else torch.cuda.current_stream(self.dev_err.device)
+        if self.concurrent:
+            fork = torch.cuda.Event()
+            fork.record(main)
         for j, layer in enumerate(wl.layers):
             blocks, nvalid, mb = (self.blocks_src, self.nvalid_src, self.Kp) if j == 0 else (self.blocks,
                                                                                             self.nvalid, self.K)
+            on = main
+            if self.concurrent and j > 0:
+                on = self.side[j - 1]
+                on.wait_event(fork)
             ci.ci_select_sparse(layer.q_fp4, layer.q_sf, layer.w, layer.k_pool, blocks=blocks, nvalid=nvalid,
                                 max_blocks=mb, topk=self.P, out_pos=self.pos[j],
-                                out_score=None if self.score is None else self.score[j], **common)
+                                out_score=None if self.score is None else self.score[j],
+                                **dict(common, stream=on))
+            if not self.concurrent:
+                mark("select")
+        if self.concurrent:
+            for side in self.side:
+                joined = torch.cuda.Event()
+                joined.record(side)
+                main.wait_event(joined)
             mark("select")
 
     def outputs_numpy(self):
