@@ -128,17 +128,28 @@ def score_positions(q, w, k, kscale):
     return w64 @ r, np.abs(w64) @ r
 
 
-def row_operands(layer, page_table, layout, t):
+def request_of(layout, t, row_req=None):
+    """The request whose pages row ``t`` reads: itself for decode rows (layout
+    0), request 0 for a one-request prefill chunk (layout 1), ``row_req[t]``
+    for a chunk of several requests (layout 2; sglang PR #40352, Design: the
+    chunk's rows carry their request starts and per-request rows)."""
+    if layout == 0:
+        return t
+    if layout == 1:
+        return 0
+    return int(row_req[t])
+
+
+def row_operands(layer, page_table, layout, t, row_req=None):
     """Decoded query, weights and page-table row of row ``t`` of one layer."""
     q = decode_query(np.asarray(layer.q_fp4[t]), np.asarray(layer.q_sf[t]))
     w = np.asarray(layer.w[t], dtype=np.float64)
-    req = t if layout == 0 else 0
-    return q, w, np.asarray(page_table[req])
+    return q, w, np.asarray(page_table[request_of(layout, t, row_req)])
 
 
-def dense_row_scores(layer, page_table, layout, t, L):
+def dense_row_scores(layer, page_table, layout, t, L, row_req=None):
     """Scores and tolerance magnitudes of every position ``s < L`` of row ``t``."""
-    q, w, prow = row_operands(layer, page_table, layout, t)
+    q, w, prow = row_operands(layer, page_table, layout, t, row_req)
     pos = np.arange(L, dtype=np.int64)
     k, ks = gather_keys(layer.k_pool, prow, pos)
     return score_positions(q, w, k, ks)
@@ -201,31 +212,46 @@ def candidate_positions(blocks, nvalid: int, L: int):
     return pos[pos < L]
 
 
-def sparse_row_scores(layer, page_table, layout, t, positions):
+def sparse_row_scores(layer, page_table, layout, t, positions, row_req=None):
     """Scores and tolerance magnitudes of row ``t`` at the given positions."""
-    q, w, prow = row_operands(layer, page_table, layout, t)
+    q, w, prow = row_operands(layer, page_table, layout, t, row_req)
     k, ks = gather_keys(layer.k_pool, prow, positions)
     return score_positions(q, w, k, ks)
 
 
-def select_row(layer, page_table, layout, t, L, blocks, nvalid, P):
+def select_row(layer, page_table, layout, t, L, blocks, nvalid, P, row_req=None):
     """A layer's top-``P`` positions of row ``t`` inside its candidate blocks.
 
     Returns ``(positions[P], candidate_positions, scores, tolmag)`` where the
     last three describe every candidate position, for tolerance checks.
     """
     pos = candidate_positions(blocks, nvalid, L)
-    logit, tolmag = sparse_row_scores(layer, page_table, layout, t, pos)
+    logit, tolmag = sparse_row_scores(layer, page_table, layout, t, pos, row_req)
     return top_positions(logit, pos, P), pos, logit, tolmag
 
 
 # ----------------------------------------------------------------------------- one row, both levels
-def source_row(layer, page_table, layout, t, L, K, P):
+def source_row(layer, page_table, layout, t, L, K, P, row_req=None):
     """The source layer's work for row ``t``: dense scores, block keys, the
     published top-``K`` blocks and its own dense top-``P`` positions."""
-    logit, tolmag = dense_row_scores(layer, page_table, layout, t, L)
+    logit, tolmag = dense_row_scores(layer, page_table, layout, t, L, row_req)
     keys, arg = block_keys(logit, L)
     nb = num_blocks(L)
     blocks, nvalid = select_blocks(keys, nb, K)
     own = top_positions(logit, np.arange(L), P)
     return dict(logit=logit, tolmag=tolmag, keys=keys, key_arg=arg, blocks=blocks, nvalid=nvalid, top=own)
+
+
+def prefill_tail_rows(req_start, tail_lens):
+    """The rows ``prefill_tail`` keeps, in order: the last ``tail_lens[r]``
+    rows of each request ``r`` (fewer when the request has fewer rows)
+    (sglang PR #40352, Design: prefill_tail restricts what was published to
+    the last rows of each request, for the late layers that run on the tail
+    only)."""
+    rows = []
+    for r in range(len(req_start) - 1):
+        lo, hi = int(req_start[r]), int(req_start[r + 1])
+        n = min(max(int(tail_lens[r]), 0), hi - lo)
+        rows.extend(range(hi - n, hi))
+    return np.asarray(rows, dtype=np.int64)
+

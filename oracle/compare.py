@@ -136,10 +136,11 @@ def check_step(wl, out, rows=None, rep=None):
     Kp = P + 1
     rows = range(wl.rows) if rows is None else rows
     seq = wl.seq_len.numpy()
+    row_req = wl.row_req()
     for t in rows:
         L = int(seq[t])
         nb = O.num_blocks(L)
-        logit, tolmag = O.dense_row_scores(wl.layers[0], pt, layout, t, L)
+        logit, tolmag = O.dense_row_scores(wl.layers[0], pt, layout, t, L, row_req)
         if nb > min(K, Kp):
             keys, arg = check_keys(rep, f"row {t} keys", out["keys"][t], L, logit, tolmag)
         else:
@@ -155,7 +156,7 @@ def check_step(wl, out, rows=None, rep=None):
         blocks = np.asarray(out["blocks"][t], dtype=np.int64)
         nv = int(out["nvalid"][t])
         for j in range(1, len(wl.layers)):
-            _, cand, sc, tm = O.select_row(wl.layers[j], pt, layout, t, L, blocks, nv, P)
+            _, cand, sc, tm = O.select_row(wl.layers[j], pt, layout, t, L, blocks, nv, P, row_req)
             check_positions(rep, f"row {t} layer {j}", out["pos"][j][t], None if score is None else score[j][t],
                             cand, sc, tm, P)
         rep.stats["rows"] += 1

@@ -176,6 +176,63 @@ def test_page_table_indirection_is_transparent():
         assert np.array_equal(O.dense_row_scores(moved, pt, 0, t, L)[0], base[t])
 
 
+def _concat_requests(a, b):
+    """A two-request chunk made of two one-request workloads: rows of `a`
+    then rows of `b`, b's pages moved after a's in one pool."""
+    pa = a.layers[0].k_pool.shape[0]
+    pta, ptb = a.page_table.numpy(), b.page_table.numpy()
+    width = max(pta.shape[1], ptb.shape[1])
+    pt = np.full((2, width), -1, dtype=np.int32)
+    pt[0, : pta.shape[1]] = pta[0]
+    pt[1, : ptb.shape[1]] = np.where(ptb[0] >= 0, ptb[0] + pa, -1)
+    layers = [synth.Layer(torch.cat([la.q_fp4, lb.q_fp4]), torch.cat([la.q_sf, lb.q_sf]), torch.cat([la.w, lb.w]),
+                          torch.cat([la.k_pool, lb.k_pool])) for la, lb in zip(a.layers, b.layers)]
+    starts = torch.tensor([0, a.rows, a.rows + b.rows], dtype=torch.int32)
+    return synth.Workload("ab", synth.LAYOUT_VARLEN, torch.cat([a.seq_len, b.seq_len]), torch.from_numpy(pt), layers,
+                          a.topk_blocks, a.topk, starts)
+
+
+def test_varlen_rows_read_their_own_request():
+    # Rows of a multi-request chunk must score exactly as the same rows of
+    # their own one-request chunk: wrong request or page-table row fails.
+    a = synth.make_workload("a", synth.LAYOUT_PREFILL, [300, 301, 302], 8, seed=21, layers=2)
+    b = synth.make_workload("b", synth.LAYOUT_PREFILL, [700, 701], 8, seed=22, layers=2)
+    ab = _concat_requests(a, b)
+    rr = ab.row_req()
+    assert rr.tolist() == [0, 0, 0, 1, 1]
+    pt = ab.page_table.numpy()
+    for t in range(ab.rows):
+        src, u = (a, t) if t < a.rows else (b, t - a.rows)
+        L = int(src.seq_len[u])
+        for j in range(2):
+            want = O.dense_row_scores(src.layers[j], src.page_table.numpy(), synth.LAYOUT_PREFILL, u, L)[0]
+            got = O.dense_row_scores(ab.layers[j], pt, synth.LAYOUT_VARLEN, t, L, rr)[0]
+            assert np.array_equal(got, want), (t, j)
+
+
+def test_varlen_builder_groups_rows_by_request():
+    wl = synth.make_varlen_workload("v", [100, 3000, 20], [3, 5, 2], 16, seed=1, layers=1)
+    assert wl.req_start.tolist() == [0, 3, 8, 10]
+    assert wl.seq_len.tolist() == [101, 102, 103, 3001, 3002, 3003, 3004, 3005, 21, 22]
+    pt = wl.page_table.numpy()
+    used = np.concatenate([pt[r][pt[r] >= 0] for r in range(3)])
+    assert len(set(used.tolist())) == used.size  # no page shared between requests
+    assert [int((pt[r] >= 0).sum()) for r in range(3)] == [2, 47, 1]
+
+
+@pytest.mark.parametrize("starts,tails,want", [
+    ([0, 3, 8, 10], [1, 2, 5], [2, 6, 7, 8, 9]),      # tail longer than its request keeps all its rows
+    ([0, 4, 4, 6], [0, 3, 1], [5]),                   # empty tail, empty request
+    ([0, 2], [2], [0, 1]),
+])
+def test_prefill_tail_rows_definition(starts, tails, want):
+    # brute force: a row is kept iff it is among the last tails[r] rows of its request
+    brute = [t for r in range(len(starts) - 1) for t in range(starts[r], starts[r + 1])
+             if t >= starts[r + 1] - max(tails[r], 0)]
+    assert brute == want
+    assert O.prefill_tail_rows(starts, tails).tolist() == want
+
+
 # ----------------------------------------------------------------------------- level one
 def test_block_keys_fixture():
     (L,), scores, expect = _read_fixture("amax8_contract.txt")

@@ -40,6 +40,7 @@ PAGE_VALUE_BYTES = PAGE * D
 PAGE_BYTES = PAGE * D + PAGE * 4
 LAYOUT_DECODE = 0
 LAYOUT_PREFILL = 1
+LAYOUT_VARLEN = 2  # a prefill chunk of several requests: rows req_start[r] .. req_start[r + 1] - 1 are request r
 TOPK_POSITIONS = 512
 
 
@@ -60,6 +61,16 @@ class Workload:
     layers: list  # [source, consumer_1, ..., consumer_4]
     topk_blocks: int
     topk: int = TOPK_POSITIONS
+    req_start: torch.Tensor = None  # int32 [num_req + 1] (LAYOUT_VARLEN only)
+
+    def row_req(self):
+        """numpy int64 [rows]: the request of every row (LAYOUT_VARLEN), else None."""
+        if self.layout != LAYOUT_VARLEN:
+            return None
+        import numpy as np
+
+        starts = self.req_start.cpu().numpy().astype(np.int64)
+        return np.repeat(np.arange(len(starts) - 1), np.diff(starts))
 
     @property
     def rows(self) -> int:
@@ -83,6 +94,7 @@ class Workload:
             [Layer(mv(l.q_fp4), mv(l.q_sf), mv(l.w), mv(l.k_pool)) for l in self.layers],
             self.topk_blocks,
             self.topk,
+            None if self.req_start is None else mv(self.req_start),
         )
 
 
@@ -168,6 +180,46 @@ def make_workload(name: str, layout: int, seq_len, topk_blocks: int, seed: int, 
                               cpu_gen)
             l.k_pool.copy_(pool_cpu)
     return Workload(name, layout, seq_len.to(device), page_table.to(device), ls, topk_blocks, topk)
+
+
+def make_varlen_workload(name: str, prefixes, rows_per_req, topk_blocks: int, seed: int, layers: int = 5,
+                         device="cpu", topk: int = TOPK_POSITIONS) -> Workload:
+    """A prefill chunk of several requests: request r contributes
+    rows_per_req[r] causal rows after a prefix of prefixes[r] compressed
+    positions (row i of the request reaches prefixes[r] + i + 1 positions).
+    Every request has its own pages (random physical order) in one pool per
+    layer; rows are grouped by request."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    lens, starts = [], [0]
+    for pre, n in zip(prefixes, rows_per_req):
+        lens.extend(int(pre) + i + 1 for i in range(int(n)))
+        starts.append(starts[-1] + int(n))
+    seq_len = torch.as_tensor(lens, dtype=torch.int32)
+    rows = int(seq_len.shape[0])
+    pages_per = [(int(pre) + int(n) + PAGE - 1) // PAGE for pre, n in zip(prefixes, rows_per_req)]
+    num_pages = max(sum(pages_per), 1)
+    max_pages = max(max(pages_per) if pages_per else 0, 1)
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(seed + 7919))
+    page_table = torch.full((len(pages_per), max_pages), -1, dtype=torch.int32)
+    off = 0
+    for r, n in enumerate(pages_per):
+        page_table[r, :n] = perm[off : off + n].to(torch.int32)
+        off += n
+    ls = [_layer(rows, num_pages, gen, device) for _ in range(layers)]
+    return Workload(name, LAYOUT_VARLEN, seq_len.to(device), page_table.to(device), ls, topk_blocks, topk,
+                    torch.as_tensor(starts, dtype=torch.int32).to(device))
+
+
+# A multi-request prefill chunk of 16384 rows: four requests of 4096 rows each
+# after prefixes of 16 K, 64 K, 128 K and 240 K compressed positions.
+VARLEN_CHUNK = dict(name="varlen_prefill_4x4096rows_prefix16k-240k_K2048",
+                    prefixes=(16384, 65536, 131072, 245760), rows_per_req=(4096, 4096, 4096, 4096), topk_blocks=2048,
+                    seed=5)
+
+
+def varlen_chunk_workload(device="cpu", layers: int = 5) -> Workload:
+    return make_varlen_workload(device=device, layers=layers, **VARLEN_CHUNK)
 
 
 def _uniform_lengths(rows, lo, hi, seed):
