@@ -45,6 +45,16 @@
  *      CI_LAYOUT_DECODE  row t is request t (num_req == rows);
  *      CI_LAYOUT_PREFILL all rows belong to request 0 (num_req == 1) and share
  *                        its pages; row t reaches its first L_t positions.
+ *      CI_LAYOUT_VARLEN  a prefill chunk of several requests: rows
+ *                        req_row_start[r] .. req_row_start[r+1]-1 belong to
+ *                        request r and read its pages (sglang PR #40352,
+ *                        Design: the chunk's inputs carry request starts and
+ *                        rows per request).  req_row_start: device int32
+ *                        [num_req + 1], 0 = req_row_start[0] <= ... <=
+ *                        req_row_start[num_req] = rows, 1 <= num_req <= 4096;
+ *                        ignored (may be NULL) for the other layouts.  A
+ *                        violation found on the device sets CI_DEVERR_REQ.
+ *    Output positions are request-relative in every layout.
  *  - seq_len int32 [rows]: L_t, with 0 <= L_t <= max_len <= 64 * max_pages.
  *    max_len is the caller's host-side bound; the kernels check every L_t
  *    against it on the device.
@@ -90,13 +100,14 @@ enum ci_status {
   CI_ERR_CUDA = -6         /* a CUDA call failed (launch or attribute) */
 };
 
-enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1 };
+enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1, CI_LAYOUT_VARLEN = 2 };
 
 /* Bits OR-ed into *dev_err by the kernels. */
 #define CI_DEVERR_LEN 1u     /* seq_len[t] < 0 or > max_len */
 #define CI_DEVERR_PAGE 2u    /* page id outside [0, num_pages) */
 #define CI_DEVERR_BLOCK 4u   /* candidate block id outside [0, ceil(L_t/8)) or nvalid out of range */
 #define CI_DEVERR_TIMEOUT 8u /* an on-chip pipeline wait gave up (should never happen) */
+#define CI_DEVERR_REQ 16u    /* req_row_start is not a partition of the rows (CI_LAYOUT_VARLEN) */
 
 /*
  * Level one, scoring: block keys of the source layer.
@@ -116,7 +127,8 @@ enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1 };
  */
 CI_API int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                          int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
-                         int32_t layout, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                         int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
+                         int32_t max_len,
                          int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
                          void* stream);
 
@@ -179,7 +191,8 @@ CI_API int ci_publish_blocks2(const int32_t* seq_len, int32_t rows, int32_t max_
  */
 CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                      int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
-                     int32_t layout, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                     int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
+                     int32_t max_len,
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
                      int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
                      void* stream);

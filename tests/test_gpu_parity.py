@@ -197,6 +197,12 @@ def subset_workload(wl_dev, rows):
     """The sampled rows' operands on the CPU (the whole pool comes along)."""
     idx = torch.tensor(rows, dtype=torch.long, device=wl_dev.seq_len.device)
     layers = [synth.Layer(l.q_fp4[idx].cpu(), l.q_sf[idx].cpu(), l.w[idx].cpu(), l.k_pool.cpu()) for l in wl_dev.layers]
+    if wl_dev.layout == synth.LAYOUT_VARLEN:
+        # every sampled row becomes a one-row request that reads its own request's pages
+        req = torch.as_tensor(wl_dev.row_req()[rows], dtype=torch.long)
+        starts = torch.arange(len(rows) + 1, dtype=torch.int32)
+        return synth.Workload(wl_dev.name, wl_dev.layout, wl_dev.seq_len[idx].cpu(), wl_dev.page_table.cpu()[req],
+                              layers, wl_dev.topk_blocks, wl_dev.topk, starts)
     pt = wl_dev.page_table[idx].cpu() if wl_dev.layout == synth.LAYOUT_DECODE else wl_dev.page_table.cpu()
     return synth.Workload(wl_dev.name, wl_dev.layout, wl_dev.seq_len[idx].cpu(), pt, layers, wl_dev.topk_blocks,
                           wl_dev.topk)
@@ -260,3 +266,45 @@ def test_positions_without_scores_match_with_scores(ci, cid):
     assert int(a.dev_err.item()) == 0 and int(b.dev_err.item()) == 0
     assert torch.equal(a.pos, b.pos)
     assert torch.equal(a.blocks, b.blocks) and torch.equal(a.blocks_src, b.blocks_src)
+
+
+@needs_cuda
+@pytest.mark.parametrize("prefixes,rows_per_req,K", [
+    ((300, 2040, 0, 5000), (4, 1, 2, 5), 64),     # requests of 1, 2, 4 and 5 rows: ragged row triples
+    ((3000, 3000, 100), (3, 3, 3), 200),           # equal requests, one short enough to keep all its blocks
+    ((20000,), (7,), 2048),                        # a single request through the several-requests layout
+])
+def test_varlen_prefill_all_rows(ci, prefixes, rows_per_req, K):
+    wl = synth.make_varlen_workload("var", prefixes, rows_per_req, K, seed=303)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+@needs_cuda
+def test_varlen_bad_row_starts_flag_without_fault(ci):
+    wl = synth.make_varlen_workload("bad", (500, 700), (3, 3), 16, seed=7)
+    dev = wl.to("cuda")
+    dev.req_start[1] = 7  # beyond the rows: not a partition
+    from two_level_sparse_gb300.step import IndexerStep
+
+    step = IndexerStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) & ci.DEVERR_REQ
+
+
+@needs_cuda
+def test_varlen_chunk_sampled_rows(ci):
+    """A 16384-row chunk of four requests (prefixes 16 K - 240 K) in the
+    benchmark's launch configuration, checked on rows at every request edge."""
+    wl_dev = synth.varlen_chunk_workload(device="cuda")
+    step = run_step(None, wl_dev=wl_dev)
+    assert int(step.dev_err.item()) == 0
+    starts = wl_dev.req_start.tolist()
+    rows = sorted({r for s0 in starts[:-1] for r in (s0, s0 + 1, s0 + 2)} | {s1 - 1 for s1 in starts[1:]} | {9000})
+    sub = subset_workload(wl_dev, rows)
+    out = step.outputs_numpy()
+    sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
+    assert_ok(compare.check_step(sub, sub_out))
+

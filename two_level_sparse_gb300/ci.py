@@ -25,18 +25,19 @@ CI_ERR = {
 }
 LAYOUT_DECODE = 0
 LAYOUT_PREFILL = 1
-DEVERR_LEN, DEVERR_PAGE, DEVERR_BLOCK, DEVERR_TIMEOUT = 1, 2, 4, 8
+LAYOUT_VARLEN = 2
+DEVERR_LEN, DEVERR_PAGE, DEVERR_BLOCK, DEVERR_TIMEOUT, DEVERR_REQ = 1, 2, 4, 8, 16
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 
 SIGNATURES = {
-    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
+    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
     "ci_publish_blocks": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P, _P],
     "ci_publish_blocks2": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _P],
-    "ci_select_sparse": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _I32, _I32, _P, _I64, _P, _I32, _I32, _P, _P,
-                         _I64, _P, _P],
+    "ci_select_sparse": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32, _P,
+                         _P, _I64, _P, _P],
     "ci_strerror": [ctypes.c_int],
     "ci_version": [],
 }
@@ -95,8 +96,14 @@ def _expect(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _req_start(layout, req_start):
+    if int(layout) == LAYOUT_VARLEN:
+        _expect(req_start, torch.int32, "req_start")
+    return _ptr(req_start)
+
+
 def ci_score_dense_amax8(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, skip_le_blocks, keys,
-                         dev_err=None, stream=None):
+                         dev_err=None, stream=None, req_start=None):
     """Block keys of the source layer (see include/ci.h)."""
     for t, d, n in ((q_fp4, torch.uint8, "q_fp4"), (q_sf, torch.uint8, "q_sf"), (w, torch.float32, "w"),
                     (k_pool, torch.uint8, "k_pool"), (page_table, torch.int32, "page_table"),
@@ -105,9 +112,9 @@ def ci_score_dense_amax8(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, ma
     rows = int(seq_len.shape[0])
     _check("ci_score_dense_amax8", lib.ci_score_dense_amax8(
         _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), _ptr(page_table),
-        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _ptr(seq_len), rows, int(max_len),
-        int(skip_le_blocks), _ptr(keys), int(keys.stride(0)) if keys.dim() == 2 else 0, _ptr(dev_err),
-        _stream(stream)))
+        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
+        rows, int(max_len), int(skip_le_blocks), _ptr(keys), int(keys.stride(0)) if keys.dim() == 2 else 0,
+        _ptr(dev_err), _stream(stream)))
 
 
 def ci_publish_blocks(seq_len, max_len, keys, topk_blocks, blocks, nvalid, dev_err=None, stream=None):
@@ -137,7 +144,7 @@ def ci_publish_blocks2(seq_len, max_len, keys, topk_blocks, blocks, nvalid, topk
 
 
 def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, blocks, nvalid, max_blocks, topk,
-                     out_pos, out_score=None, dev_err=None, stream=None):
+                     out_pos, out_score=None, dev_err=None, stream=None, req_start=None):
     """A layer's top-k positions inside the candidate blocks (see include/ci.h)."""
     for t, d, n in ((q_fp4, torch.uint8, "q_fp4"), (q_sf, torch.uint8, "q_sf"), (w, torch.float32, "w"),
                     (k_pool, torch.uint8, "k_pool"), (page_table, torch.int32, "page_table"),
@@ -149,6 +156,6 @@ def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_le
     rows = int(seq_len.shape[0])
     _check("ci_select_sparse", lib.ci_select_sparse(
         _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), _ptr(page_table),
-        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _ptr(seq_len), rows, int(max_len),
-        _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(topk), _ptr(out_pos),
+        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
+        rows, int(max_len), _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(topk), _ptr(out_pos),
         _ptr(out_score), int(out_pos.stride(0)), _ptr(dev_err), _stream(stream)))

@@ -57,14 +57,19 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Checks shared by the two scoring entry points.
 int check_pool(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool, int64_t num_pages,
-               const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout, const int32_t* seq_len,
-               int32_t rows, int32_t max_len) {
+               const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
+               const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len) {
   if (rows < 0 || max_len < 0 || num_pages < 0 || num_req < 0 || max_pages < 0) return CI_ERR_SHAPE;
-  if (layout != CI_LAYOUT_DECODE && layout != CI_LAYOUT_PREFILL) return CI_ERR_UNSUPPORTED;
+  if (layout != CI_LAYOUT_DECODE && layout != CI_LAYOUT_PREFILL && layout != CI_LAYOUT_VARLEN)
+    return CI_ERR_UNSUPPORTED;
   if (rows == 0) return CI_OK;
   if (!q_fp4 || !q_sf || !w || !k_pool || !page_table || !seq_len) return CI_ERR_NULL;
   if (layout == CI_LAYOUT_DECODE && num_req != rows) return CI_ERR_SHAPE;
   if (layout == CI_LAYOUT_PREFILL && num_req != 1) return CI_ERR_SHAPE;
+  if (layout == CI_LAYOUT_VARLEN) {
+    if (!req_row_start) return CI_ERR_NULL;
+    if (num_req < 1 || num_req > ci::kMaxReq) return CI_ERR_RANGE;
+  }
   if (static_cast<int64_t>(max_len) > static_cast<int64_t>(max_pages) * CI_PAGE) return CI_ERR_SHAPE;
   if (num_pages < 1 || num_pages > INT32_MAX) return CI_ERR_RANGE;
   if (!aligned(k_pool, 16) || !aligned(q_fp4, 8) || !aligned(q_sf, 16) || !aligned(w, 16)) return CI_ERR_ALIGN;
@@ -77,7 +82,7 @@ int launched(cudaError_t e) { return e == cudaSuccess ? CI_OK : CI_ERR_CUDA; }
 
 extern "C" {
 
-int ci_version(void) { return 100; }
+int ci_version(void) { return 101; }
 
 const char* ci_strerror(int status) {
   switch (status) {
@@ -94,17 +99,19 @@ const char* ci_strerror(int status) {
 
 int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                          int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
-                         int32_t layout, const int32_t* seq_len, int32_t rows, int32_t max_len,
-                         int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err, void* stream) {
-  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, seq_len, rows,
-                      max_len);
+                         int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
+                         int32_t max_len, int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
+                         void* stream) {
+  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, req_row_start,
+                      seq_len, rows, max_len);
   if (st != CI_OK) return st;
   if (skip_le_blocks < 0) return CI_ERR_RANGE;
   if (rows == 0) return CI_OK;
   if (!keys) return CI_ERR_NULL;
   if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
   if (!aligned(keys, 16)) return CI_ERR_ALIGN;
-  ci::DenseArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, seq_len, rows, max_len, dev_err},
+  ci::DenseArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, req_row_start, num_req, seq_len,
+                   rows, max_len, dev_err},
                   skip_le_blocks,
                   keys,
                   keys_stride};
@@ -141,11 +148,12 @@ int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, con
 
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                      int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
-                     const int32_t* seq_len, int32_t rows, int32_t max_len, const int32_t* blocks,
-                     int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks, int32_t topk, int32_t* out_pos,
-                     float* out_score, int64_t out_stride, int32_t* dev_err, void* stream) {
-  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, seq_len, rows,
-                      max_len);
+                     const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                     const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
+                     int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
+                     void* stream) {
+  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, req_row_start,
+                      seq_len, rows, max_len);
   if (st != CI_OK) return st;
   if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
   if (max_blocks < 0 || max_blocks > 2176) return CI_ERR_RANGE;
@@ -153,7 +161,8 @@ int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, 
   if (rows == 0) return CI_OK;
   if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
   if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;
-  ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, seq_len, rows, max_len, dev_err},
+  ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, req_row_start, num_req, seq_len,
+                    rows, max_len, dev_err},
                    blocks,
                    blocks_stride,
                    nvalid,

@@ -14,7 +14,8 @@ constexpr int kPage = 64;
 constexpr int kPageValueBytes = kPage * kDim;          // 8192
 constexpr int kPageBytes = kPageValueBytes + kPage * 4;  // 8448
 constexpr int kTileM = 128;                            // positions per MMA tile
-constexpr uint32_t kDevErrLen = 1u, kDevErrPage = 2u, kDevErrBlock = 4u, kDevErrTimeout = 8u;
+constexpr uint32_t kDevErrLen = 1u, kDevErrPage = 2u, kDevErrBlock = 4u, kDevErrTimeout = 8u, kDevErrReq = 16u;
+constexpr int kLayoutDecode = 0, kLayoutPrefill = 1, kLayoutVarlen = 2;
 
 __device__ __forceinline__ void report(int32_t* dev_err, uint32_t bits) {
   if (dev_err != nullptr) atomicOr(reinterpret_cast<unsigned int*>(dev_err), bits);

@@ -6,6 +6,8 @@
 
 namespace ci {
 
+constexpr int kMaxReq = 4096;  // requests of one multi-request chunk (layout 2)
+
 struct PoolArgs {
   const uint8_t* q_fp4;
   const uint8_t* q_sf;
@@ -14,7 +16,9 @@ struct PoolArgs {
   int64_t num_pages;
   const int32_t* page_table;
   int32_t max_pages;
-  int32_t layout;  // 0 decode (row t = request t), 1 prefill (one request)
+  int32_t layout;  // 0 decode (row t = request t), 1 prefill (one request), 2 several requests
+  const int32_t* req_start;  // layout 2: rows of request r are [req_start[r], req_start[r + 1])
+  int32_t num_req;
   const int32_t* seq_len;
   int32_t rows;
   int32_t max_len;

@@ -55,6 +55,7 @@ struct __align__(1024) Smem {
   int g_begin, o_begin;
   long long t_begin, t_end;
   long long warp_sum[kThreads / 32];
+  int32_t gpre[kMaxReq + 1];  // several requests: groups of requests < r
 };
 
 // Length that row `row` is scored over: L if it has more than skip_le_blocks
@@ -65,14 +66,34 @@ __device__ __forceinline__ int scored_len(const DenseArgs& a, int row) {
   return ((L + kBlock - 1) / kBlock) > a.skip_le_blocks ? L : 0;
 }
 
+// Group g: up to R consecutive rows of one request, sharing its pages.
+struct RowGroup {
+  int req, first, count;
+};
 template <int R>
-__device__ __forceinline__ int group_len(const DenseArgs& a, int g) {
+__device__ __forceinline__ RowGroup row_group(const DenseArgs& a, const int32_t* gpre, int g) {
+  if (a.p.layout == kLayoutVarlen) {
+    int lo = 0, hi = a.p.num_req;  // the request r with gpre[r] <= g < gpre[r + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (gpre[mid] <= g)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int first = __ldg(a.p.req_start + lo) + R * (g - gpre[lo]);
+    return {lo, first, min(R, __ldg(a.p.req_start + lo + 1) - first)};
+  }
+  const int first = g * R;
+  return {a.p.layout == kLayoutPrefill ? 0 : g, first, min(R, a.p.rows - first)};
+}
+
+template <int R>
+__device__ __forceinline__ int group_len(const DenseArgs& a, const RowGroup& grp) {
   int m = 0;
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int r = g * R + i;
-    if (r < a.p.rows) m = max(m, scored_len(a, r));
-  }
+  for (int i = 0; i < R; ++i)
+    if (i < grp.count) m = max(m, scored_len(a, grp.first + i));
   return m;
 }
 
@@ -95,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int num_groups = (a.p.rows + R - 1) / R;
   volatile int* abort_flag = &sm.abort_flag;
 
   // ---------------------------------------------------------------- set-up
@@ -124,16 +144,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Several requests: groups per request (checked row starts), their prefix.
+  int num_groups = (a.p.rows + R - 1) / R;
+  if (a.p.layout == kLayoutVarlen) {
+    constexpr int kPer = (kMaxReq + kThreads - 1) / kThreads;
+    int cnt[kPer], local = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int r = tid * kPer + j;
+      cnt[j] = 0;
+      if (r < a.p.num_req) {
+        const int s0 = a.p.req_start[r], s1 = a.p.req_start[r + 1];
+        const bool ok = 0 <= s0 && s0 <= s1 && s1 <= a.p.rows && (r > 0 || s0 == 0) &&
+                        (r < a.p.num_req - 1 || s1 == a.p.rows);
+        if (!ok && blockIdx.x == 0) report(a.p.dev_err, kDevErrReq);
+        cnt[j] = ok ? (s1 - s0 + R - 1) / R : 0;
+      }
+      local += cnt[j];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.warp_sum[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) before += static_cast<int>(sm.warp_sum[w]);
+      total += static_cast<int>(sm.warp_sum[w]);
+    }
+    int run = before + incl - local;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int r = tid * kPer + j;
+      if (r < a.p.num_req) sm.gpre[r] = run;
+      run += cnt[j];
+    }
+    if (tid == 0) sm.gpre[a.p.num_req] = total;
+    num_groups = total;
+    __syncthreads();
+  }
   // Work split: this CTA's share of the (group, tile) list.
   {
     const int per = (num_groups + kThreads - 1) / kThreads;
     const int g0 = min(num_groups, tid * per), g1 = min(num_groups, g0 + per);
     long long mine = 0;
     for (int g = g0; g < g1; ++g) {
+      const RowGroup grp = row_group<R>(a, sm.gpre, g);
       if (blockIdx.x == 0)
-        for (int r = g * R; r < min(a.p.rows, g * R + R); ++r)
-          if (scored_len(a, r) < 0) report(a.p.dev_err, kDevErrLen);
-      mine += (group_len<R>(a, g) + kTileM - 1) / kTileM;
+        for (int i = 0; i < grp.count; ++i)
+          if (scored_len(a, grp.first + i) < 0) report(a.p.dev_err, kDevErrLen);
+      mine += (group_len<R>(a, grp) + kTileM - 1) / kTileM;
     }
     long long incl = mine;
 #pragma unroll
@@ -160,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tb < te && excl <= tb && tb < excl + mine) {
       long long acc = excl;
       for (int g = g0; g < g1; ++g) {
-        const int n = (group_len<R>(a, g) + kTileM - 1) / kTileM;
+        const int n = (group_len<R>(a, row_group<R>(a, sm.gpre, g)) + kTileM - 1) / kTileM;
         if (tb < acc + n) {
           sm.g_begin = g;
           sm.o_begin = static_cast<int>(tb - acc);
@@ -189,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned long long w2[32];  // head weights, packed pairs
 
   while (remaining > 0 && g < num_groups) {
-    const int glen = group_len<R>(a, g);
+    const RowGroup grp = row_group<R>(a, sm.gpre, g);
+    const int glen = group_len<R>(a, grp);
     const int ntiles = (glen + kTileM - 1) / kTileM;
     const int take = static_cast<int>(min(static_cast<long long>(ntiles - off), remaining));
     if (take <= 0) {
@@ -202,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- group set-up: queries widened to e4m3 in the swizzled B tile
     for (int idx = tid; idx < N * 8; idx += kThreads) {
       const int n = idx >> 3, c = idx & 7;
-      const int row = g * R + n / kHeads, head = n % kHeads;
+      const int row = grp.first + n / kHeads, head = n % kHeads;
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < a.p.rows) {
+      if (n / kHeads < grp.count) {
         const uint2 packed =
             *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(row) * kHeads + head) * 64 + c * 8);
         v = widen_fp4x16(packed);
@@ -218,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int n = 32 * c + lane;
-        const int row = g * R + n / kHeads, head = n % kHeads;
-        sf[c] = (n < N && row < a.p.rows)
+        const int row = grp.first + n / kHeads, head = n % kHeads;
+        sf[c] = (n < N && n / kHeads < grp.count)
                     ? *reinterpret_cast<const uint32_t*>(a.p.q_sf + (static_cast<int64_t>(row) * kHeads + head) * 4)
                     : kUnitScales;
       }
@@ -230,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: this warpgroup's row and its head weights
     int row = -1, rlen = 0;
     if (epi >= 0) {
-      row = R == 3 ? g * 3 + epi : g;
+      const int i = R == 3 ? epi : 0;
+      row = i < grp.count ? grp.first + i : a.p.rows;
       if (row < a.p.rows) {
         rlen = max(scored_len(a, row), 0);  // 0 when the row is skipped: nothing is stored
         load_head_weights(w2, a.p.w + static_cast<int64_t>(row) * kHeads);
@@ -242,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA producer
-      const int req = a.p.layout == 1 ? 0 : g;
+      const int req = grp.req;
       const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
       const int end = off + take;
       uint32_t ts = tseq;
@@ -385,7 +450,7 @@ cudaError_t launch_dense_amax8(const DenseArgs& a, cudaStream_t stream) {
   cudaError_t e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, kPage);
   if (e != cudaSuccess) return e;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
-  if (a.p.layout == 1) {
+  if (a.p.layout != kLayoutDecode) {
     e = cudaFuncSetAttribute(dense_amax8_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dense_amax8_kernel<3><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);

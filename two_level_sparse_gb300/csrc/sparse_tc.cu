@@ -92,6 +92,22 @@ __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
   report(dev_err, kDevErrTimeout);
 }
 
+// The request whose pages row `row` reads (several requests: the last r
+// with req_start[r] <= row).
+__device__ __forceinline__ int row_request(const SelectArgs& a, int row) {
+  if (a.p.layout == kLayoutDecode) return row;
+  if (a.p.layout == kLayoutPrefill) return 0;
+  int lo = 0, hi = a.p.num_req;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a.p.req_start + mid) <= row)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
 struct RowInfo {
   int row, L, nv, nb, ntiles;
 };
@@ -151,7 +167,7 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
   fence_proxy_async_smem();
   mbar_arrive(&sm.q_full[b]);
   ok = ok && warp_wait(&sm.info_empty[b], ph ^ 1, abort_flag);  // row ri - 2 gathered and scored
-  const int req = a.p.layout == 1 ? 0 : r.row;
+  const int req = row_request(a, r.row);
   const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
   const int32_t* brow = a.blocks + static_cast<int64_t>(r.row) * a.blocks_stride;
   constexpr int kBatch = 16;

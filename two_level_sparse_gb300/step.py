@@ -74,7 +74,7 @@ class IndexerStep:
         wl = self.wl
         src = wl.layers[0]
         common = dict(page_table=wl.page_table, layout=wl.layout, seq_len=wl.seq_len, max_len=self.max_len,
-                      dev_err=self.dev_err, stream=stream)
+                      dev_err=self.dev_err, stream=stream, req_start=wl.req_start)
         if not skip_dense:
             ci.ci_score_dense_amax8(src.q_fp4, src.q_sf, src.w, src.k_pool, skip_le_blocks=self.skip, keys=self.keys,
                                     **common)
