@@ -4,7 +4,8 @@ One step = one pass of the whole indexer path over one batch of synthetic
 input: the source layer's dense block keys, its published candidate blocks,
 its own top-512 and the four consumer layers' top-512.  The headline workload
 is the 16384-row prefill chunk at 262144 compressed positions; the decode
-batches are reported as secondary lines in the same JSON object.
+batches and the multi-request prefill chunk (with prefill_tail over its
+published table) are reported as secondary lines in the same JSON object.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -294,12 +295,13 @@ def last_rows(wl, rows):
                           wl.topk_blocks, wl.topk)
 
 
-def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0):
+def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0, wl=None):
     from two_level_sparse_gb300 import synth
 
     from two_level_sparse_gb300.step import IndexerStep
 
-    wl = last_rows(synth.config_workload(cid, device="cuda"), rows)
+    if wl is None:
+        wl = last_rows(synth.config_workload(cid, device="cuda"), rows)
     step = IndexerStep(wl)
     times = time_steps(step, steps, warmup, flush, stream)
     res = {"cid": cid, "wl": wl, "step": step, "t_step": times["step"], "t_dense": times["dense"],
@@ -311,13 +313,58 @@ def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0):
     return res
 
 
+VARLEN_TAIL_ROWS = 512  # tail rows kept per request by the prefill_tail timing
+
+
+def measure_varlen(steps, stream, flush, world):
+    """The multi-request prefill chunk (four requests of 4096 rows after 16 K -
+    240 K prefixes): the whole step, then prefill_tail over its published
+    table keeping the last VARLEN_TAIL_ROWS rows of each request."""
+    from two_level_sparse_gb300 import ci, synth
+
+    wl = synth.varlen_chunk_workload(device="cuda")
+    r = measure(None, steps, 3, stream, flush, wl=wl)
+    step = r["step"]
+    nreq = wl.req_start.shape[0] - 1
+    tail_len = torch.full((nreq,), VARLEN_TAIL_ROWS, dtype=torch.int32, device="cuda")
+    cap = nreq * VARLEN_TAIL_ROWS
+    out_row = torch.empty(cap, dtype=torch.int32, device="cuda")
+    out_blocks = torch.empty(cap, step.K, dtype=torch.int32, device="cuda")
+    out_nvalid = torch.empty(cap, dtype=torch.int32, device="cuda")
+    out_count = torch.empty(1, dtype=torch.int32, device="cuda")
+    tail_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ci.ci_prefill_tail(wl.req_start, tail_len, step.blocks, step.nvalid, out_row, out_blocks, out_nvalid,
+                               out_count, dev_err=step.dev_err, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                tail_ms.append(e0.elapsed_time(e1))
+    mst = statistics.mean(r["t_step"])
+    tail = statistics.mean(tail_ms)
+    moved = cap * (step.K + 2) * 4 * 2  # rows read and written, with their count and source row
+    return {
+        "metric": "multi-request prefill chunk ms", "workload": wl.name, "value": mst, "unit": "ms",
+        "rows_per_s": world * wl.rows / (mst * 1e-3), "ms_per_step": mst,
+        "kernel_ms": {"dense": statistics.mean(r["t_dense"]), "publish": statistics.mean(r["t_publish"]),
+                      "select": statistics.mean(r["t_select"])},
+        "prefill_tail": {"ms": tail, "rows_kept": int(out_count.item()), "tail_rows_per_request": VARLEN_TAIL_ROWS,
+                         "bytes": moved, "gbs": moved / (tail * 1e-3) / 1e9},
+        "dev_err": int(step.dev_err.item()),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-secondary", action="store_true", help="skip the decode workloads")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the decode and multi-request workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--rows", type=int, default=0,
@@ -387,6 +434,8 @@ def main():
             })
             del r
             torch.cuda.empty_cache()
+        secondary.append(measure_varlen(max(3, args.steps // 2), stream, flush, world))
+        torch.cuda.empty_cache()
 
     cpu_ms, cpu_rows, cpu_threads, nrows = (None, 0, 0, 0)
     if rank == 0 and not args.no_cpu:

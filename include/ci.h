@@ -17,6 +17,8 @@
  *     ci_publish_blocks2     the same for two block counts at once (the
  *                            consumers' K and the source's own P + 1),
  *                            reading the keys once;
+ *     ci_prefill_tail        the published table of the last rows of each
+ *                            request of a multi-request chunk;
  *   level two, once per layer (the source itself and each consumer):
  *     ci_select_sparse       scores only the positions inside a row's
  *                            published blocks and returns its top-k positions,
@@ -166,6 +168,28 @@ CI_API int ci_publish_blocks2(const int32_t* seq_len, int32_t rows, int32_t max_
                        int64_t keys_stride, int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride,
                        int32_t* nvalid, int32_t topk_blocks2, int32_t* blocks2, int64_t blocks2_stride,
                        int32_t* nvalid2, int32_t* dev_err, void* stream);
+
+/*
+ * The published table restricted to the tail rows of each request (sglang
+ * PR #40352, Design: prefill_tail restricts what was published to the last
+ * rows of each request, for the late layers that run on the tail only).
+ *
+ * Request r owns rows req_row_start[r] .. req_row_start[r+1]-1 (the
+ * CI_LAYOUT_VARLEN partition) and keeps its last m_r = min(max(tail_len[r],
+ * 0), its row count) rows.  The kept rows, in order, become output rows
+ * 0 .. M-1 (M = sum of m_r, written to *out_count): for each output row o,
+ * out_row[o] = its source row, out_blocks[o * out_blocks_stride + i] =
+ * blocks[out_row[o] * blocks_stride + i] for i < topk_blocks, out_nvalid[o] =
+ * nvalid[out_row[o]].  Output rows M .. out_cap-1 get out_row -1, nvalid 0
+ * and INT32_MAX ids.  If M > out_cap only the first out_cap are written and
+ * CI_DEVERR_REQ is set, as it is for row starts that are not a partition.
+ * req_row_start: int32 [num_req + 1], 1 <= num_req <= 4096; tail_len: int32
+ * [num_req]; all device memory.
+ */
+CI_API int ci_prefill_tail(const int32_t* req_row_start, int32_t num_req, const int32_t* tail_len, int32_t rows,
+                    const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t topk_blocks,
+                    int32_t* out_row, int32_t* out_blocks, int64_t out_blocks_stride, int32_t* out_nvalid,
+                    int32_t* out_count, int32_t out_cap, int32_t* dev_err, void* stream);
 
 /*
  * Level two: a layer's top-k positions inside the candidate blocks.

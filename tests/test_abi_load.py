@@ -29,8 +29,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(
-        ["ci_publish_blocks", "ci_publish_blocks2", "ci_score_dense_amax8", "ci_select_sparse", "ci_strerror",
-         "ci_version"])
+        ["ci_prefill_tail", "ci_publish_blocks", "ci_publish_blocks2", "ci_score_dense_amax8", "ci_select_sparse",
+         "ci_strerror", "ci_version"])
 
 
 def test_library_exports_every_declared_symbol(ci):
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(ci):
 
 
 def test_status_names(ci):
-    assert ci.version() == 101
+    assert ci.version() == 102
     assert ci.strerror(0) == "ok"
     for code in ci.CI_ERR:
         assert ci.strerror(code) != "unknown status"
@@ -95,6 +95,38 @@ def test_publish_pair_host_checks(ci):
     assert f(P, 2, 64, P, 8, 16, P, 16, P, 20, P, 16, P, N, N) == -2  # blocks2 stride < topk_blocks2
     assert f(P, 2, 64, P, 8, 16, P, 16, P, 4, P, 4, N, N, N) == -1  # nvalid2 missing
     assert f(P, 2, 64, P, 8, 0, P, 16, P, 4, N, 4, N, N, N) == -4  # first selection checked as before
+
+
+def test_prefill_tail_host_checks(ci):
+    f = ci.lib.ci_prefill_tail
+    ok_args = [P, 2, P, 64, P, 16, P, 16, P, P, 16, P, P, 8, N, N]
+    bad = list(ok_args)
+    bad[1] = 0  # no request
+    assert f(*bad) == -4
+    bad = list(ok_args)
+    bad[1] = 4097  # too many requests
+    assert f(*bad) == -4
+    bad = list(ok_args)
+    bad[7] = 0  # topk_blocks < 1
+    assert f(*bad) == -4
+    bad = list(ok_args)
+    bad[13] = -1  # negative capacity
+    assert f(*bad) == -2
+    bad = list(ok_args)
+    bad[10] = 8  # output stride < topk_blocks
+    assert f(*bad) == -2
+    bad = list(ok_args)
+    bad[5] = 8  # input stride < topk_blocks
+    assert f(*bad) == -2
+    bad = list(ok_args)
+    bad[0] = N  # no row starts
+    assert f(*bad) == -1
+    bad = list(ok_args)
+    bad[12] = N  # no count
+    assert f(*bad) == -1
+    bad = list(ok_args)
+    bad[9] = N  # capacity but no output table
+    assert f(*bad) == -1
 
 
 def test_select_host_checks(ci):

@@ -308,3 +308,85 @@ def test_varlen_chunk_sampled_rows(ci):
     sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
     assert_ok(compare.check_step(sub, sub_out))
 
+
+
+def run_tail(ci, rows_per_req, tail_lens, K, cap, seed):
+    """ci_prefill_tail over a seeded table of block ids (any int32 values:
+    the op only moves rows); returns the table, its counts and the outputs."""
+    g = torch.Generator().manual_seed(seed)
+    starts = torch.zeros(len(rows_per_req) + 1, dtype=torch.int32)
+    starts[1:] = torch.cumsum(torch.as_tensor(rows_per_req, dtype=torch.int32), 0)
+    rows = int(starts[-1])
+    blocks = torch.randint(-2**31, 2**31 - 1, (rows, K), generator=g, dtype=torch.int32)
+    nvalid = torch.randint(0, K + 1, (rows,), generator=g, dtype=torch.int32)
+    dev = dict(req_start=starts.cuda(), tail_len=torch.as_tensor(tail_lens, dtype=torch.int32).cuda(),
+               blocks=blocks.cuda(), nvalid=nvalid.cuda())
+    out_row = torch.full((cap,), 12345, dtype=torch.int32, device="cuda")
+    out_blocks = torch.full((cap, K), 12345, dtype=torch.int32, device="cuda")
+    out_nvalid = torch.full((cap,), 12345, dtype=torch.int32, device="cuda")
+    out_count = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ci.ci_prefill_tail(dev["req_start"], dev["tail_len"], dev["blocks"], dev["nvalid"], out_row, out_blocks, out_nvalid,
+                       out_count, dev_err=dev_err)
+    torch.cuda.synchronize()
+    return (starts.numpy(), blocks.numpy(), nvalid.numpy(), out_row.cpu().numpy(), out_blocks.cpu().numpy(),
+            out_nvalid.cpu().numpy(), int(out_count.item()), int(dev_err.item()))
+
+
+@needs_cuda
+@pytest.mark.parametrize("rows_per_req,tail_lens,K,extra", [
+    ((5, 1, 0, 7, 300), (2, 3, 4, 7, 129), 16, 0),        # tail shorter, longer, empty request, whole, long
+    ((4, 4, 4), (0, -3, 4), 2048, 5),                     # nothing kept, negative length, spare capacity padded
+    ((1,) * 4096, tuple(i % 2 for i in range(4096)), 64, 3),  # the most requests: every other one kept
+    ((16384,), (4096,), 2048, 0),                         # one long request, the tail a quarter of it
+])
+def test_prefill_tail_gathers_tail_rows_bit_exact(ci, rows_per_req, tail_lens, K, extra):
+    starts, blocks, nvalid, _, _, _, _, _ = run_tail(ci, rows_per_req, tail_lens, K, 0, seed=11)
+    want = O.prefill_tail_rows(starts, tail_lens)
+    cap = len(want) + extra
+    _, _, _, out_row, out_blocks, out_nvalid, count, err = run_tail(ci, rows_per_req, tail_lens, K, cap, seed=11)
+    assert err == 0 and count == len(want)
+    np.testing.assert_array_equal(out_row[:count], want)
+    np.testing.assert_array_equal(out_blocks[:count], blocks[want])
+    np.testing.assert_array_equal(out_nvalid[:count], nvalid[want])
+    assert (out_row[count:] == -1).all() and (out_nvalid[count:] == 0).all()
+    assert (out_blocks[count:] == 0x7FFFFFFF).all()
+
+
+@needs_cuda
+def test_prefill_tail_short_capacity_flags_and_writes_the_first_rows(ci):
+    rows_per_req, tail_lens = (10, 20, 30), (5, 10, 15)
+    starts, blocks, nvalid, out_row, out_blocks, out_nvalid, count, err = run_tail(ci, rows_per_req, tail_lens, 32, 12,
+                                                                                   seed=3)
+    want = O.prefill_tail_rows(starts, tail_lens)
+    assert count == len(want) == 30 and err & ci.DEVERR_REQ
+    np.testing.assert_array_equal(out_row, want[:12])
+    np.testing.assert_array_equal(out_blocks, blocks[want[:12]])
+    np.testing.assert_array_equal(out_nvalid, nvalid[want[:12]])
+
+
+@needs_cuda
+def test_prefill_tail_after_a_varlen_step_matches_the_oracle(ci):
+    """The tail of a real multi-request chunk: the gathered candidate blocks of
+    each tail row are the oracle's selection for that row."""
+    wl = synth.make_varlen_workload("tail", (300, 2040, 5000), (4, 9, 5), 64, seed=21)
+    dev = wl.to("cuda")
+    step = run_step(None, wl_dev=dev)
+    tail_lens = torch.tensor([2, 9, 0], dtype=torch.int32, device="cuda")
+    want = O.prefill_tail_rows(wl.req_start.numpy(), tail_lens.cpu().numpy()).tolist()
+    n = len(want)
+    out_row = torch.empty(n, dtype=torch.int32, device="cuda")
+    out_blocks = torch.empty(n, step.blocks.shape[1], dtype=torch.int32, device="cuda")
+    out_nvalid = torch.empty(n, dtype=torch.int32, device="cuda")
+    out_count = torch.empty(1, dtype=torch.int32, device="cuda")
+    ci.ci_prefill_tail(dev.req_start, tail_lens, step.blocks, step.nvalid, out_row, out_blocks, out_nvalid, out_count,
+                       dev_err=step.dev_err)
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) == 0 and int(out_count.item()) == n
+    assert out_row.cpu().tolist() == want
+    sub = subset_workload(dev, want)
+    out = step.outputs_numpy()
+    sub_out = {k: (v[:, want] if k in ("pos", "score") else v[want]) for k, v in out.items()}
+    sub_out["blocks"] = out_blocks.cpu().numpy()
+    sub_out["nvalid"] = out_nvalid.cpu().numpy()
+    assert_ok(compare.check_step(sub, sub_out))

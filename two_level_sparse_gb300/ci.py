@@ -36,6 +36,7 @@ SIGNATURES = {
     "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
     "ci_publish_blocks": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P, _P],
     "ci_publish_blocks2": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _P],
+    "ci_prefill_tail": [_P, _I32, _P, _I32, _P, _I64, _P, _I32, _P, _P, _I64, _P, _P, _I32, _P, _P],
     "ci_select_sparse": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32, _P,
                          _P, _I64, _P, _P],
     "ci_strerror": [ctypes.c_int],
@@ -141,6 +142,22 @@ def ci_publish_blocks2(seq_len, max_len, keys, topk_blocks, blocks, nvalid, topk
         _ptr(seq_len), rows, int(max_len), _ptr(keys), int(keys.stride(0)), int(topk_blocks), _ptr(blocks),
         int(blocks.stride(0)), _ptr(nvalid), int(topk_blocks2), _ptr(blocks2), int(blocks2.stride(0)), _ptr(nvalid2),
         _ptr(dev_err), _stream(stream)))
+
+
+def ci_prefill_tail(req_start, tail_len, blocks, nvalid, out_row, out_blocks, out_nvalid, out_count, dev_err=None,
+                    stream=None):
+    """The published table of the last rows of each request (see include/ci.h)."""
+    for t, n in ((req_start, "req_start"), (tail_len, "tail_len"), (blocks, "blocks"), (nvalid, "nvalid"),
+                 (out_row, "out_row"), (out_blocks, "out_blocks"), (out_nvalid, "out_nvalid"),
+                 (out_count, "out_count")):
+        _expect(t, torch.int32, n)
+    num_req = int(req_start.shape[0]) - 1
+    if int(tail_len.shape[0]) != num_req:
+        raise ValueError("tail_len needs one entry per request")
+    _check("ci_prefill_tail", lib.ci_prefill_tail(
+        _ptr(req_start), num_req, _ptr(tail_len), int(blocks.shape[0]), _ptr(blocks), int(blocks.stride(0)),
+        _ptr(nvalid), int(blocks.shape[1]), _ptr(out_row), _ptr(out_blocks), int(out_blocks.stride(0)),
+        _ptr(out_nvalid), _ptr(out_count), int(out_blocks.shape[0]), _ptr(dev_err), _stream(stream)))
 
 
 def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, blocks, nvalid, max_blocks, topk,

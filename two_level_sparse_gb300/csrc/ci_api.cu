@@ -82,7 +82,7 @@ int launched(cudaError_t e) { return e == cudaSuccess ? CI_OK : CI_ERR_CUDA; }
 
 extern "C" {
 
-int ci_version(void) { return 101; }
+int ci_version(void) { return 102; }
 
 const char* ci_strerror(int status) {
   switch (status) {
@@ -144,6 +144,21 @@ int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_len, con
                       void* stream) {
   return ci_publish_blocks2(seq_len, rows, max_len, keys, keys_stride, topk_blocks, blocks, blocks_stride, nvalid, 0,
                             nullptr, 0, nullptr, dev_err, stream);
+}
+
+int ci_prefill_tail(const int32_t* req_row_start, int32_t num_req, const int32_t* tail_len, int32_t rows,
+                    const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t topk_blocks,
+                    int32_t* out_row, int32_t* out_blocks, int64_t out_blocks_stride, int32_t* out_nvalid,
+                    int32_t* out_count, int32_t out_cap, int32_t* dev_err, void* stream) {
+  if (rows < 0 || out_cap < 0) return CI_ERR_SHAPE;
+  if (num_req < 1 || num_req > ci::kMaxReq) return CI_ERR_RANGE;
+  if (topk_blocks < 1 || topk_blocks > 16384) return CI_ERR_RANGE;
+  if (!req_row_start || !tail_len || !out_count) return CI_ERR_NULL;
+  if (out_cap > 0 && (!blocks || !nvalid || !out_row || !out_blocks || !out_nvalid)) return CI_ERR_NULL;
+  if (blocks_stride < topk_blocks || out_blocks_stride < topk_blocks) return CI_ERR_SHAPE;
+  ci::TailArgs a{req_row_start, num_req, tail_len,   rows,    blocks,    blocks_stride, nvalid, topk_blocks,
+                 out_row,       out_blocks, out_blocks_stride, out_nvalid, out_count, out_cap, dev_err};
+  return launched(ci::launch_tail(a, static_cast<cudaStream_t>(stream)));
 }
 
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,

@@ -63,7 +63,26 @@ struct SelectArgs {
 
 // Each returns a cudaError_t from the launch (cudaSuccess when enqueued).
 cudaError_t launch_dense_amax8(const DenseArgs& a, cudaStream_t stream);
+struct TailArgs {
+  const int32_t* req_start;
+  int32_t num_req;
+  const int32_t* tail_len;
+  int32_t rows;
+  const int32_t* blocks;
+  int64_t blocks_stride;
+  const int32_t* nvalid;
+  int32_t topk_blocks;
+  int32_t* out_row;
+  int32_t* out_blocks;
+  int64_t out_blocks_stride;
+  int32_t* out_nvalid;
+  int32_t* out_count;
+  int32_t out_cap;
+  int32_t* dev_err;
+};
+
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
+cudaError_t launch_tail(const TailArgs& a, cudaStream_t stream);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 
 // Shared host helpers (ci_api.cu).
