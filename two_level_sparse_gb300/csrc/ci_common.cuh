@@ -83,16 +83,17 @@ __device__ __forceinline__ bool warp_wait_fast(uint64_t* bar, uint32_t parity, v
 struct HeadAcc {
   unsigned long long p[4];
 };
-__device__ __forceinline__ void relu_fma_pair(unsigned long long& acc, unsigned long long w2, uint32_t x0,
-                                              uint32_t x1) {
-  asm("{\n\t.reg .f32 r0, r1;\n\t.reg .b64 c;\n\t"
-      "max.f32 r0, %2, 0f00000000;\n\tmax.f32 r1, %3, 0f00000000;\n\t"
-      "mov.b64 c, {r0, r1};\n\tfma.rn.f32x2 %0, %1, c, %0;\n\t}"
-      : "+l"(acc)
-      : "l"(w2), "r"(x0), "r"(x1));
+// (The ReLU is taken in place: x0, x1 are consumed.)
+__device__ __forceinline__ void relu_fma_pair(unsigned long long& acc, unsigned long long w2, uint32_t& x0,
+                                              uint32_t& x1) {
+  asm("{\n\t.reg .b64 c;\n\t"
+      "max.f32 %1, %1, 0f00000000;\n\tmax.f32 %2, %2, 0f00000000;\n\t"
+      "mov.b64 c, {%1, %2};\n\tfma.rn.f32x2 %0, %3, c, %0;\n\t}"
+      : "+l"(acc), "+r"(x0), "+r"(x1)
+      : "l"(w2));
 }
 // x: heads 32 half .. 32 half + 31 of the position; w2: their 16 weight pairs.
-__device__ __forceinline__ void head_reduce_half(HeadAcc& acc, const uint32_t (&x)[32], const unsigned long long* w2) {
+__device__ __forceinline__ void head_reduce_half(HeadAcc& acc, uint32_t (&x)[32], const unsigned long long* w2) {
 #pragma unroll
   for (int m = 0; m < 16; ++m) relu_fma_pair(acc.p[m & 3], w2[m], x[2 * m], x[2 * m + 1]);
 }
