@@ -4,8 +4,9 @@ One step = one pass of the whole indexer path over one batch of synthetic
 input: the source layer's dense block keys, its published candidate blocks,
 its own top-512 and the four consumer layers' top-512.  The headline workload
 is the 16384-row prefill chunk at 262144 compressed positions; the decode
-batches and the multi-request prefill chunk (with prefill_tail over its
-published table) are reported as secondary lines in the same JSON object.
+batches, the multi-request prefill chunk (with prefill_tail over its
+published table) and the headline chunk with MXFP4 index-K pools are reported
+as secondary lines in the same JSON object.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -121,27 +122,35 @@ def algorithmic_counts(wl):
     """FLOPs of the dense pass and bytes of index-K it must read.
 
     Dense scorer: 2 * H * D flops per (row, position) over rows with more than
-    min(K, P + 1) blocks.  Bytes: 132 per position of K (128 e4m3 + 4-byte scale) read
-    once per launch -- the pool of a prefill chunk, every scored row's own
-    positions in decode -- plus the query and weights of scored rows.
+    min(K, P + 1) blocks.  Bytes: 132 per position of K (128 e4m3 + 4-byte scale;
+    68 for MXFP4 pools: 64 packed bytes + 4 scale bytes) read once per launch --
+    the pool of a prefill chunk, every scored row's own positions in decode --
+    plus the query and weights of scored rows.
     """
+    kpos = k_position_bytes(wl)
     L = wl.seq_len.to(torch.int64).cpu()
     nb = (L + 7) // 8
     scored = nb > min(wl.topk_blocks, wl.topk + 1)
     positions = int(L[scored].sum())
     flops = 2 * 64 * 128 * positions
     if wl.layout == 1:
-        kbytes = 132 * (int(L.max()) if bool(scored.any()) else 0)
+        kbytes = kpos * (int(L.max()) if bool(scored.any()) else 0)
     else:
-        kbytes = 132 * positions
+        kbytes = kpos * positions
     qbytes = int(scored.sum()) * (64 * 64 + 64 * 4 + 64 * 4)
     return flops, kbytes + qbytes, positions
+
+
+def k_position_bytes(wl):
+    """Index-K bytes per position: 132 for FP8 pages, 68 for MXFP4 pages."""
+    return 68 if wl.kv == 1 else 132
 
 
 def select_bytes(wl):
     """Algorithmic bytes of the step's five sparse-scorer launches.
 
-    Per candidate position 132 bytes (128 e4m3 + one fp32 scale) gathered; per
+    Per candidate position 132 bytes (128 e4m3 + one fp32 scale; 68 for MXFP4
+    pools) gathered; per
     row and launch the query, its scales and weights (4608 bytes), the block
     ids (4 per block) and the output positions (4 per pick).  A row with
     nb_t <= K' blocks scores all L_t positions; otherwise K' - 1 full blocks
@@ -156,7 +165,7 @@ def select_bytes(wl):
         full = nb > kb
         pos = torch.where(full, 8 * (kb - 1) + (L - 8 * (nb - 1)), L)
         blocks = torch.where(full, torch.full_like(nb, kb), nb)
-        return int((132 * pos + 4608 + 4 * blocks + 4 * P).sum())
+        return int((k_position_bytes(wl) * pos + 4608 + 4 * blocks + 4 * P).sum())
 
     return one(P + 1) + (len(wl.layers) - 1) * one(K)
 
@@ -313,6 +322,34 @@ def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0, wl=None):
     return res
 
 
+def measure_mxfp4(steps, stream, flush, world, peaks):
+    """The headline chunk with MXFP4 index-K pools (the pages' use_fp4_cache
+    variant): the same step with FP4 x FP4 block-scaled MMAs and 68-byte K
+    positions."""
+    from two_level_sparse_gb300 import synth
+
+    wl = synth.config_workload(HEADLINE_CID, device="cuda", kv=synth.KV_MXFP4)
+    r = measure(None, steps, 3, stream, flush, wl=wl)
+    mst, msd, mss = (statistics.mean(r[k]) for k in ("t_step", "t_dense", "t_select"))
+    flops, _, _ = algorithmic_counts(wl)
+    sel = select_bytes(wl)
+    fp4_peak = 4.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    line = {
+        "metric": "indexer ms per 16K-token prefill chunk @262K ctx, MXFP4 index-K", "workload": wl.name,
+        "value": mst, "unit": "ms", "ms_per_step": mst,
+        "kernel_ms": {"dense": msd, "publish": statistics.mean(r["t_publish"]), "select": mss},
+        "dense_roofline": {"bound": "tensor", "achieved": flops / (msd * 1e-3) / 1e12, "peak": fp4_peak,
+                           "unit": "TFLOP/s", "frac": flops / (msd * 1e-3) / 1e12 / fp4_peak,
+                           "peak_source": "bf16_tflops_sustained x4 (fp4 / bf16 nominal ratio)"},
+        "select_roofline": {"bound": "hbm", "achieved": sel / (mss * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": sel / (mss * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                            "bytes_per_step": sel},
+        "dev_err": int(r["step"].dev_err.item()),
+    }
+    del r
+    return line
+
+
 VARLEN_TAIL_ROWS = 512  # tail rows kept per request by the prefill_tail timing
 
 
@@ -364,7 +401,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-secondary", action="store_true", help="skip the decode and multi-request workloads")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the decode, multi-request and MXFP4 workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--rows", type=int, default=0,
@@ -435,6 +472,8 @@ def main():
             del r
             torch.cuda.empty_cache()
         secondary.append(measure_varlen(max(3, args.steps // 2), stream, flush, world))
+        torch.cuda.empty_cache()
+        secondary.append(measure_mxfp4(max(3, args.steps // 2), stream, flush, world, peaks))
         torch.cuda.empty_cache()
 
     cpu_ms, cpu_rows, cpu_threads, nrows = (None, 0, 0, 0)

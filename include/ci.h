@@ -35,11 +35,20 @@
  *    element 2i in the low nibble; q_sf uint8 [rows][64][4], one ue8m0 scale
  *    per 32 elements (vLLM sparse_attn_indexer.py, "MXFP4 layout" comment).
  *  - Head weights: w float [rows][64].
- *  - Index-K pool: k_pool uint8 [num_pages][8448].  Page p holds 64 positions:
- *    bytes [0, 8192) are their FP8 e4m3 vectors (128 bytes each), bytes
- *    [8192, 8448) their fp32 scales (little endian).  The scale multiplies the
- *    decoded vector.  k_pool, q_sf and w must be 16-byte aligned, q_fp4 8-byte
- *    aligned.
+ *  - Index-K pool, in one of two page formats (`kv_format`):
+ *      CI_KV_FP8    k_pool uint8 [num_pages][8448].  Page p holds 64
+ *                   positions: bytes [0, 8192) are their FP8 e4m3 vectors
+ *                   (128 bytes each), bytes [8192, 8448) their fp32 scales
+ *                   (little endian).  The scale multiplies the decoded vector.
+ *      CI_KV_MXFP4  k_pool uint8 [num_pages][4352].  Bytes [0, 4096) are the
+ *                   64 positions' MXFP4 vectors (64 bytes each, two e2m1
+ *                   codes per byte, element 2i in the low nibble), bytes
+ *                   [4096, 4352) one 32-bit word per position whose byte j is
+ *                   the ue8m0 scale of elements 32j .. 32j + 31 (vLLM
+ *                   sparse_attn_indexer.py, _gather_workspace_shapes and
+ *                   kv_cache_as_quant_view, the use_fp4_cache path: head_dim/2
+ *                   packed bytes and head_dim/32 ue8m0 scales per position).
+ *    k_pool, q_sf and w must be 16-byte aligned, q_fp4 8-byte aligned.
  *  - Page table: page_table int32 [num_req][max_pages]; logical page j of a
  *    request lives in physical page page_table[req][j].  Position s of a row
  *    is slot s % 64 of logical page s / 64.
@@ -91,6 +100,7 @@ extern "C" {
 #define CI_BLOCK 8
 #define CI_PAGE 64
 #define CI_PAGE_BYTES (CI_PAGE * CI_DIM + CI_PAGE * 4)
+#define CI_PAGE_BYTES_MXFP4 (CI_PAGE * CI_DIM / 2 + CI_PAGE * 4)
 
 enum ci_status {
   CI_OK = 0,
@@ -103,6 +113,7 @@ enum ci_status {
 };
 
 enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1, CI_LAYOUT_VARLEN = 2 };
+enum ci_kv_format { CI_KV_FP8 = 0, CI_KV_MXFP4 = 1 };
 
 /* Bits OR-ed into *dev_err by the kernels. */
 #define CI_DEVERR_LEN 1u     /* seq_len[t] < 0 or > max_len */
@@ -118,7 +129,8 @@ enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1, CI_LAYOUT_VARLEN =
  * b < nb_t writes
  *     keys[t * keys_stride + b] = max_{8b <= s < min(8b + 8, L_t)} logit[t, s]
  * with logit[t, s] = kscale[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s]) computed in
- * fp32 (products exact, fp32 accumulation), and keys[t*keys_stride + nb_t - 1]
+ * fp32 (products exact, fp32 accumulation; kscale = 1 for CI_KV_MXFP4, whose
+ * scales are part of k), and keys[t*keys_stride + nb_t - 1]
  * = +inf.  Rows with nb_t <= skip_le_blocks are not scored and their keys are
  * left untouched (sglang PR #40352, Design, "Level one"; the block_amax.cuh
  * listing in the same PR's review: max of 8, last key +inf, rows with at most
@@ -128,7 +140,7 @@ enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1, CI_LAYOUT_VARLEN =
  * keys_stride >= ceil(max_len / 8).
  */
 CI_API int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
-                         int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                         int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
                          int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
                          int32_t max_len,
                          int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
@@ -214,7 +226,7 @@ CI_API int ci_prefill_tail(const int32_t* req_row_start, int32_t num_req, const 
  * 1 <= topk <= 2048, topk <= out_stride; num_pages <= 2^24.
  */
 CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
-                     int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                     int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
                      int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
                      int32_t max_len,
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,

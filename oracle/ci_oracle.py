@@ -14,7 +14,10 @@ What it computes follows these passages:
   ``fp8_fp4_paged_mqa_logits`` calls).  The per-position fp32 K scale
   multiplies the decoded e4m3 vector; the ue8m0 query scale multiplies each
   32-element block of the decoded e2m1 query (same file, "MXFP4 layout"
-  comment and ``_gather_workspace_shapes``).
+  comment and ``_gather_workspace_shapes``).  With the MXFP4 index-K cache
+  (the same file's ``use_fp4_cache`` path: ``head_dim / 2`` packed bytes and
+  ``head_dim / 32`` ue8m0 scales per position) K is decoded exactly like the
+  query and there is no per-position scale (it is 1).
 * level one -- one key per block of 8 positions, the maximum score inside the
   block; the row's newest block is forced to +inf so it is always kept; rows
   with at most ``K`` blocks keep every block (PR #40352, Design, "Level one";
@@ -42,6 +45,8 @@ BLOCK = 8
 PAGE = 64
 PAGE_VALUE_BYTES = PAGE * D
 PAGE_BYTES = PAGE_VALUE_BYTES + PAGE * 4
+PAGE_VALUE_BYTES_MXFP4 = PAGE * D // 2
+PAGE_BYTES_MXFP4 = PAGE_VALUE_BYTES_MXFP4 + PAGE * 4
 INT32_MAX = 2**31 - 1
 
 # Magnitudes of the eight e2m1 codes (sign in bit 3), as tabulated by the OCP
@@ -85,7 +90,8 @@ def decode_e4m3(codes) -> np.ndarray:
 
 
 def decode_query(q_fp4_row, q_sf_row) -> np.ndarray:
-    """One row's MXFP4 query ``[H, D/2]`` + ``[H, D/32]`` -> float64 ``[H, D]``."""
+    """MXFP4 vectors ``[..., D/2]`` + ``[..., D/32]`` -> float64 ``[..., D]``
+    (one row's query, or MXFP4 K vectors)."""
     vals = decode_e2m1(unpack_fp4(q_fp4_row))
     scale = np.repeat(decode_ue8m0(q_sf_row), 32, axis=-1)
     return vals * scale
@@ -101,14 +107,35 @@ def page_values_and_scales(k_pool):
     return vals, scales
 
 
+def page_values_and_scales_mxfp4(k_pool):
+    """Views of a ``[num_pages, PAGE_BYTES_MXFP4]`` pool: packed e2m1 bytes
+    ``[pages, 64, 64]`` and ue8m0 scale bytes ``[pages, 64, 4]`` (byte ``j`` of
+    a position scales its elements ``32j .. 32j + 31``)."""
+    pool = np.ascontiguousarray(np.asarray(k_pool, dtype=np.uint8))
+    pages = pool.reshape(-1, PAGE_BYTES_MXFP4)
+    vals = pages[:, :PAGE_VALUE_BYTES_MXFP4].reshape(-1, PAGE, D // 2)
+    scales = pages[:, PAGE_VALUE_BYTES_MXFP4:].reshape(-1, PAGE, D // 32)
+    return vals, scales
+
+
+def is_mxfp4_pool(k_pool) -> bool:
+    return np.asarray(k_pool).shape[-1] == PAGE_BYTES_MXFP4
+
+
 def gather_keys(k_pool, page_row, positions):
-    """Decoded K vectors ``[n, D]`` and fp32 scales ``[n]`` at logical positions
-    of one request, read through its page-table row."""
-    vals, scales = page_values_and_scales(k_pool)
+    """Decoded K vectors ``[n, D]`` and per-position scales ``[n]`` at logical
+    positions of one request, read through its page-table row.  An FP8 pool
+    gives e4m3 vectors and their fp32 scales; an MXFP4 pool gives e2m1 vectors
+    with their ue8m0 block scales applied, and scales of 1."""
     positions = np.asarray(positions, dtype=np.int64)
     page_row = np.asarray(page_row, dtype=np.int64)
     phys = page_row[positions // PAGE]
     off = positions % PAGE
+    if is_mxfp4_pool(k_pool):
+        vals, scales = page_values_and_scales_mxfp4(k_pool)
+        k = decode_query(vals[phys, off], scales[phys, off])
+        return k, np.ones(len(positions), dtype=np.float64)
+    vals, scales = page_values_and_scales(k_pool)
     k = decode_e4m3(vals[phys, off])
     ks = scales[phys, off].astype(np.float64)
     return k, ks

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(ci):
 
 
 def test_status_names(ci):
-    assert ci.version() == 102
+    assert ci.version() == 200
     assert ci.strerror(0) == "ok"
     for code in ci.CI_ERR:
         assert ci.strerror(code) != "unknown status"
@@ -54,28 +54,30 @@ N = None
 def test_dense_host_checks(ci):
     f = ci.lib.ci_score_dense_amax8
     # rows == 0: nothing to do, even with null pointers
-    assert f(N, N, N, N, 1, N, 0, 1, 0, N, N, 0, 0, 0, N, 8, N, N) == 0
+    assert f(N, N, N, N, 1, 0, N, 0, 1, 0, N, N, 0, 0, 0, N, 8, N, N) == 0
     # null pointer
-    assert f(N, P, P, P, 1, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -1
+    assert f(N, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -1
     # bad layout
-    assert f(P, P, P, P, 1, P, 2, 1, 7, N, P, 2, 64, 0, P, 8, N, N) == -5
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 7, N, P, 2, 64, 0, P, 8, N, N) == -5
     # decode needs one request per row
-    assert f(P, P, P, P, 1, P, 3, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 3, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -2
     # prefill needs exactly one request
-    assert f(P, P, P, P, 1, P, 2, 1, 1, N, P, 2, 64, 0, P, 8, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 1, N, P, 2, 64, 0, P, 8, N, N) == -2
     # several requests: row starts required, 1..4096 requests
-    assert f(P, P, P, P, 1, P, 2, 1, 2, N, P, 2, 64, 0, P, 8, N, N) == -1
-    assert f(P, P, P, P, 1, P, 0, 1, 2, P, P, 2, 64, 0, P, 8, N, N) == -4
-    assert f(P, P, P, P, 1, P, 5000, 1, 2, P, P, 2, 64, 0, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 2, N, P, 2, 64, 0, P, 8, N, N) == -1
+    assert f(P, P, P, P, 1, 0, P, 0, 1, 2, P, P, 2, 64, 0, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 0, P, 5000, 1, 2, P, P, 2, 64, 0, P, 8, N, N) == -4
     # max_len beyond the page table
-    assert f(P, P, P, P, 1, P, 2, 1, 0, N, P, 2, 65, 0, P, 16, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 65, 0, P, 16, N, N) == -2
     # keys stride not a multiple of 8 / too short
-    assert f(P, P, P, P, 1, P, 2, 2, 0, N, P, 2, 128, 0, P, 12, N, N) == -2
-    assert f(P, P, P, P, 1, P, 2, 4, 0, N, P, 2, 256, 0, P, 8, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 2, 0, N, P, 2, 128, 0, P, 12, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 4, 0, N, P, 2, 256, 0, P, 8, N, N) == -2
     # misaligned pool
-    assert f(P, P, P, ctypes.c_void_p(0x1001), 1, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -3
+    assert f(P, P, P, ctypes.c_void_p(0x1001), 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -3
+    # unknown K page format
+    assert f(P, P, P, P, 1, 2, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -5
     # negative skip
-    assert f(P, P, P, P, 1, P, 2, 1, 0, N, P, 2, 64, -1, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, -1, P, 8, N, N) == -4
 
 
 def test_publish_host_checks(ci):
@@ -131,20 +133,23 @@ def test_prefill_tail_host_checks(ci):
 
 def test_select_host_checks(ci):
     f = ci.lib.ci_select_sparse
-    ok_args = [P, P, P, P, 1, P, 2, 1, 0, N, P, 2, 64, P, 16, P, 16, 8, P, N, 8, N, N]
-    assert f(*ok_args[:11], 0, *ok_args[12:]) == 0  # rows == 0
+    ok_args = [P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, P, 16, P, 16, 8, P, N, 8, N, N]
+    assert f(*ok_args[:12], 0, *ok_args[13:]) == 0  # rows == 0
     bad = list(ok_args)
-    bad[17] = 0  # topk < 1
+    bad[18] = 0  # topk < 1
     assert f(*bad) == -4
     bad = list(ok_args)
-    bad[16] = 5000  # max_blocks too large
+    bad[17] = 5000  # max_blocks too large
     assert f(*bad) == -4
     bad = list(ok_args)
-    bad[20] = 4  # out stride < topk
+    bad[21] = 4  # out stride < topk
     assert f(*bad) == -2
     bad = list(ok_args)
-    bad[18] = N  # no output
+    bad[19] = N  # no output
     assert f(*bad) == -1
     bad = list(ok_args)
-    bad[8] = 2  # several requests without row starts
+    bad[9] = 2  # several requests without row starts
     assert f(*bad) == -1
+    bad = list(ok_args)
+    bad[5] = 3  # unknown K page format
+    assert f(*bad) == -5

@@ -390,3 +390,85 @@ def test_prefill_tail_after_a_varlen_step_matches_the_oracle(ci):
     sub_out["blocks"] = out_blocks.cpu().numpy()
     sub_out["nvalid"] = out_nvalid.cpu().numpy()
     assert_ok(compare.check_step(sub, sub_out))
+
+
+# ----------------------------------------------------------------------------- MXFP4 index-K
+MX = synth.KV_MXFP4
+
+
+@needs_cuda
+def test_mxfp4_tiny_decode_config_all_rows(ci):
+    wl = synth.config_workload(0, kv=MX)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+@needs_cuda
+@pytest.mark.parametrize("layout,lens,K,P", [
+    (synth.LAYOUT_DECODE, [0, 1, 7, 8, 9, 100, 2100, 20000], 128, 512),
+    (synth.LAYOUT_DECODE, [5000, 5001, 4096, 4095, 65], 64, 40),
+    (synth.LAYOUT_PREFILL, [3000 + i for i in range(7)], 64, 512),
+    (synth.LAYOUT_PREFILL, [2040 + i for i in range(10)], 200, 512),
+])
+def test_mxfp4_small_all_rows(ci, layout, lens, K, P):
+    wl = synth.make_workload("mx", layout, lens, topk_blocks=K, seed=404, topk=P, kv=MX)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+@needs_cuda
+def test_mxfp4_varlen_prefill_all_rows(ci):
+    wl = synth.make_varlen_workload("mxv", (300, 2040, 0, 5000), (4, 1, 2, 5), 64, seed=505, kv=MX)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+@needs_cuda
+def test_mxfp4_dense_keys_equal_sparse_rescoring_bitwise(ci):
+    """The lemma's premise for MXFP4 pools: the sparse scorer's scores equal
+    the dense scorer's bit for bit (every block a candidate, topk >= L)."""
+    from two_level_sparse_gb300.step import IndexerStep
+
+    lens = [2000, 2001, 2002, 2040]
+    wl = synth.make_workload("lemma4", synth.LAYOUT_PREFILL, lens, topk_blocks=64, seed=6, kv=MX)
+    dev = wl.to("cuda")
+    step = IndexerStep(dev)
+    step.run()
+    rows, L = wl.rows, max(lens)
+    nb = O.num_blocks(L)
+    allb = torch.arange(nb, dtype=torch.int32, device="cuda").repeat(rows, 1).contiguous()
+    nv = torch.tensor([O.num_blocks(x) for x in lens], dtype=torch.int32, device="cuda")
+    pos = torch.empty(rows, 2048, dtype=torch.int32, device="cuda")
+    sc = torch.empty(rows, 2048, dtype=torch.float32, device="cuda")
+    src = dev.layers[0]
+    ci.ci_select_sparse(src.q_fp4, src.q_sf, src.w, src.k_pool, dev.page_table, dev.layout, dev.seq_len, L, allb, nv,
+                        nb, 2048, pos, sc)
+    torch.cuda.synchronize()
+    keys = step.keys.cpu().numpy()
+    pos, sc = pos.cpu().numpy(), sc.cpu().numpy()
+    for t, Lt in enumerate(lens):
+        assert pos[t, :Lt].tolist() == list(range(Lt)) and np.all(pos[t, Lt:] == -1)
+        for b in range(O.num_blocks(Lt) - 1):
+            assert keys[t, b].tobytes() == sc[t, 8 * b:8 * b + 8].max().tobytes(), (t, b)
+
+
+@needs_cuda
+@pytest.mark.parametrize("cid", [2, 4])
+def test_mxfp4_full_size_config_sampled_rows(ci, cid):
+    """The long-decode batch and the 16384-row chunk with MXFP4 pools, in the
+    benchmark's launch configuration, checked on sampled rows."""
+    wl_dev = synth.config_workload(cid, device="cuda", kv=MX)
+    step = run_step(None, wl_dev=wl_dev)
+    assert int(step.dev_err.item()) == 0
+    if cid == 2:
+        lens = wl_dev.seq_len.cpu()
+        rows = [int(i) for i in torch.nonzero(lens <= 16384).flatten()[:1]] + [int(torch.argmax(lens))]
+    else:
+        rows = [0, 2, 9999, 16383]
+    sub = subset_workload(wl_dev, rows)
+    out = step.outputs_numpy()
+    sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
+    assert_ok(compare.check_step(sub, sub_out))

@@ -160,6 +160,62 @@ def test_scores_match_bruteforce_loops():
         assert math.isclose(mag, tol[s], rel_tol=1e-12, abs_tol=1e-12)
 
 
+def _e2m1_value(code):
+    """OCP MX v1.0 FP4 E2M1: sign bit 3, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6."""
+    mag = {0: 0.0, 1: 0.5, 2: 1.0, 3: 1.5, 4: 2.0, 5: 3.0, 6: 4.0, 7: 6.0}[code & 7]
+    return -mag if code & 8 else mag
+
+
+def test_mxfp4_pool_layout_hand_example():
+    """One MXFP4 page built by hand: values then one scale word per position,
+    byte j of the word scaling elements 32j .. 32j + 31; read through a page
+    table that puts it second."""
+    page = np.zeros(synth.PAGE_BYTES_MXFP4, dtype=np.uint8)
+    page[0:64] = 0x71          # position 0: elements (0.5, 6.0) repeated
+    page[63 * 64 : 64 * 64] = 0x9A  # position 63: elements (-1.0, -0.5) repeated
+    base = synth.PAGE_VALUE_BYTES_MXFP4
+    page[base : base + 4] = [127, 126, 128, 125]
+    page[base + 4 * 63 : base + 4 * 64] = [120, 127, 127, 130]
+    pool = np.stack([np.zeros_like(page), page])
+    k, ks = O.gather_keys(pool, np.array([1]), np.array([0, 63]))
+    assert np.all(ks == 1.0)
+    blockscale0 = np.repeat([1.0, 0.5, 2.0, 0.25], 32)
+    want0 = np.tile([0.5, 6.0], 64) * blockscale0
+    blockscale63 = np.repeat([2.0**-7, 1.0, 1.0, 8.0], 32)
+    want63 = np.tile([-1.0, -0.5], 64) * blockscale63
+    assert np.array_equal(k[0], want0) and np.array_equal(k[1], want63)
+
+
+def test_mxfp4_scores_match_bruteforce_loops():
+    rng = np.random.default_rng(9)
+    L = 70  # two pages
+    pool = np.zeros((2, synth.PAGE_BYTES_MXFP4), dtype=np.uint8)
+    pool[:, : synth.PAGE_VALUE_BYTES_MXFP4] = rng.integers(0, 256, (2, synth.PAGE_VALUE_BYTES_MXFP4))
+    pool[:, synth.PAGE_VALUE_BYTES_MXFP4 :] = rng.integers(123, 128, (2, 256))
+    q_fp4 = rng.integers(0, 256, (synth.H, 64), dtype=np.uint8)
+    q_sf = rng.integers(123, 128, (synth.H, 4), dtype=np.uint8)
+    w = rng.normal(0, 0.125, synth.H)
+    prow = np.array([1, 0])  # logical page 0 is physical page 1
+    kk, kss = O.gather_keys(pool, prow, np.arange(L))
+    logit, tol = O.score_positions(O.decode_query(q_fp4, q_sf), w, kk, kss)
+    for s in (0, 5, 63, 64, 69):
+        phys, off = int(prow[s // 64]), s % 64
+        total, mag = 0.0, 0.0
+        for h in range(synth.H):
+            acc = 0.0
+            for d in range(synth.D):
+                qb, kb = int(q_fp4[h, d // 2]), int(pool[phys, off * 64 + d // 2])
+                qc = qb & 15 if d % 2 == 0 else qb >> 4
+                kc = kb & 15 if d % 2 == 0 else kb >> 4
+                qs = 2.0 ** (int(q_sf[h, d // 32]) - 127)
+                kscale = 2.0 ** (int(pool[phys, synth.PAGE_VALUE_BYTES_MXFP4 + 4 * off + d // 32]) - 127)
+                acc += _e2m1_value(qc) * qs * _e2m1_value(kc) * kscale
+            total += w[h] * max(acc, 0.0)
+            mag += abs(w[h] * max(acc, 0.0))
+        assert math.isclose(total, logit[s], rel_tol=1e-12, abs_tol=1e-12)
+        assert math.isclose(mag, tol[s], rel_tol=1e-12, abs_tol=1e-12)
+
+
 def test_page_table_indirection_is_transparent():
     wl = synth.make_workload("t", synth.LAYOUT_DECODE, [150, 70], 4, seed=11, layers=1)
     layer = wl.layers[0]
@@ -392,3 +448,14 @@ def test_planted_transposed_key_index_is_caught(monkeypatch):
     monkeypatch.setattr(O, "score_positions", wrong_scale)
     with pytest.raises(AssertionError):
         test_scores_match_bruteforce_loops()
+
+
+def test_planted_mxfp4_scale_byte_order_is_caught(monkeypatch):
+    good = O.page_values_and_scales_mxfp4
+
+    def reversed_bytes(pool):
+        vals, scales = good(pool)
+        return vals, scales[..., ::-1]
+    monkeypatch.setattr(O, "page_values_and_scales_mxfp4", reversed_bytes)
+    with pytest.raises(AssertionError):
+        test_mxfp4_pool_layout_hand_example()

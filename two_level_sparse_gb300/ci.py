@@ -26,6 +26,8 @@ CI_ERR = {
 LAYOUT_DECODE = 0
 LAYOUT_PREFILL = 1
 LAYOUT_VARLEN = 2
+KV_FP8, KV_MXFP4 = 0, 1
+PAGE_BYTES = {KV_FP8: 64 * 128 + 64 * 4, KV_MXFP4: 64 * 64 + 64 * 4}
 DEVERR_LEN, DEVERR_PAGE, DEVERR_BLOCK, DEVERR_TIMEOUT, DEVERR_REQ = 1, 2, 4, 8, 16
 
 _P = ctypes.c_void_p
@@ -33,12 +35,13 @@ _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 
 SIGNATURES = {
-    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
+    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _I64, _P,
+                             _P],
     "ci_publish_blocks": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P, _P],
     "ci_publish_blocks2": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _P],
     "ci_prefill_tail": [_P, _I32, _P, _I32, _P, _I64, _P, _I32, _P, _P, _I64, _P, _P, _I32, _P, _P],
-    "ci_select_sparse": [_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32, _P,
-                         _P, _I64, _P, _P],
+    "ci_select_sparse": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32,
+                         _P, _P, _I64, _P, _P],
     "ci_strerror": [ctypes.c_int],
     "ci_version": [],
 }
@@ -97,6 +100,14 @@ def _expect(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def kv_format(k_pool) -> int:
+    """The page format of a pool, from its page size (8448 bytes: FP8, 4352: MXFP4)."""
+    for fmt, nbytes in PAGE_BYTES.items():
+        if k_pool.dim() == 2 and int(k_pool.shape[1]) == nbytes:
+            return fmt
+    raise ValueError(f"k_pool must be [num_pages, 8448] (FP8) or [num_pages, 4352] (MXFP4), got {tuple(k_pool.shape)}")
+
+
 def _req_start(layout, req_start):
     if int(layout) == LAYOUT_VARLEN:
         _expect(req_start, torch.int32, "req_start")
@@ -112,7 +123,7 @@ def ci_score_dense_amax8(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, ma
         _expect(t, d, n)
     rows = int(seq_len.shape[0])
     _check("ci_score_dense_amax8", lib.ci_score_dense_amax8(
-        _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), _ptr(page_table),
+        _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), kv_format(k_pool), _ptr(page_table),
         int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
         rows, int(max_len), int(skip_le_blocks), _ptr(keys), int(keys.stride(0)) if keys.dim() == 2 else 0,
         _ptr(dev_err), _stream(stream)))
@@ -172,7 +183,7 @@ def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_le
         _expect(out_score, torch.float32, "out_score")
     rows = int(seq_len.shape[0])
     _check("ci_select_sparse", lib.ci_select_sparse(
-        _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), _ptr(page_table),
+        _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), kv_format(k_pool), _ptr(page_table),
         int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
         rows, int(max_len), _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(topk), _ptr(out_pos),
         _ptr(out_score), int(out_pos.stride(0)), _ptr(dev_err), _stream(stream)))

@@ -35,17 +35,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-cudaError_t make_pool_tmap(CUtensorMap* map, const uint8_t* k_pool, int64_t num_pages, int box_rows) {
+cudaError_t make_pool_tmap(CUtensorMap* map, const uint8_t* k_pool, int64_t num_pages, int kv_format, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(CI_DIM), static_cast<cuuint64_t>(CI_PAGE),
-                              static_cast<cuuint64_t>(num_pages)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(CI_DIM), static_cast<cuuint64_t>(CI_PAGE_BYTES)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(CI_DIM), static_cast<cuuint32_t>(box_rows), 1};
+  // [pages][64 positions][row bytes]: 128-byte e4m3 rows (128-byte swizzle) or
+  // 64-byte packed e2m1 rows (64-byte swizzle)
+  const bool fp4 = kv_format == CI_KV_MXFP4;
+  const cuuint64_t row = fp4 ? CI_DIM / 2 : CI_DIM;
+  const cuuint64_t dims[3] = {row, static_cast<cuuint64_t>(CI_PAGE), static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[2] = {row, static_cast<cuuint64_t>(fp4 ? CI_PAGE_BYTES_MXFP4 : CI_PAGE_BYTES)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(row), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(k_pool), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -57,11 +60,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Checks shared by the two scoring entry points.
 int check_pool(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool, int64_t num_pages,
-               const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
+               int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
                const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len) {
   if (rows < 0 || max_len < 0 || num_pages < 0 || num_req < 0 || max_pages < 0) return CI_ERR_SHAPE;
   if (layout != CI_LAYOUT_DECODE && layout != CI_LAYOUT_PREFILL && layout != CI_LAYOUT_VARLEN)
     return CI_ERR_UNSUPPORTED;
+  if (kv_format != CI_KV_FP8 && kv_format != CI_KV_MXFP4) return CI_ERR_UNSUPPORTED;
   if (rows == 0) return CI_OK;
   if (!q_fp4 || !q_sf || !w || !k_pool || !page_table || !seq_len) return CI_ERR_NULL;
   if (layout == CI_LAYOUT_DECODE && num_req != rows) return CI_ERR_SHAPE;
@@ -82,7 +86,7 @@ int launched(cudaError_t e) { return e == cudaSuccess ? CI_OK : CI_ERR_CUDA; }
 
 extern "C" {
 
-int ci_version(void) { return 102; }
+int ci_version(void) { return 200; }
 
 const char* ci_strerror(int status) {
   switch (status) {
@@ -98,19 +102,19 @@ const char* ci_strerror(int status) {
 }
 
 int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
-                         int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                         int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
                          int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
                          int32_t max_len, int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
                          void* stream) {
-  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, req_row_start,
-                      seq_len, rows, max_len);
+  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, num_req, max_pages, layout,
+                      req_row_start, seq_len, rows, max_len);
   if (st != CI_OK) return st;
   if (skip_le_blocks < 0) return CI_ERR_RANGE;
   if (rows == 0) return CI_OK;
   if (!keys) return CI_ERR_NULL;
   if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
   if (!aligned(keys, 16)) return CI_ERR_ALIGN;
-  ci::DenseArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, req_row_start, num_req, seq_len,
+  ci::DenseArgs a{{q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, max_pages, layout, req_row_start, num_req, seq_len,
                    rows, max_len, dev_err},
                   skip_le_blocks,
                   keys,
@@ -162,13 +166,13 @@ int ci_prefill_tail(const int32_t* req_row_start, int32_t num_req, const int32_t
 }
 
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
-                     int64_t num_pages, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
+                     int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
                      const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len,
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
                      int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
                      void* stream) {
-  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, page_table, num_req, max_pages, layout, req_row_start,
-                      seq_len, rows, max_len);
+  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, num_req, max_pages, layout,
+                      req_row_start, seq_len, rows, max_len);
   if (st != CI_OK) return st;
   if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
   if (max_blocks < 0 || max_blocks > 2176) return CI_ERR_RANGE;
@@ -176,7 +180,7 @@ int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, 
   if (rows == 0) return CI_OK;
   if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
   if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;
-  ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, page_table, max_pages, layout, req_row_start, num_req, seq_len,
+  ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, max_pages, layout, req_row_start, num_req, seq_len,
                     rows, max_len, dev_err},
                    blocks,
                    blocks_stride,

@@ -14,11 +14,35 @@ constexpr int kPage = 64;
 constexpr int kPageValueBytes = kPage * kDim;          // 8192
 constexpr int kPageBytes = kPageValueBytes + kPage * 4;  // 8448
 constexpr int kTileM = 128;                            // positions per MMA tile
+// Index-K formats.  FP8: a page is 64 x 128 e4m3 bytes, then 64 fp32 scales.
+// MXFP4: a page is 64 x 64 bytes of packed e2m1 (element 2i in the low
+// nibble), then one 32-bit word per position whose byte j is the ue8m0 scale
+// of elements 32j .. 32j + 31.
+constexpr int kKvFp8 = 0, kKvMxfp4 = 1;
+template <int KV>
+__host__ __device__ constexpr int row_bytes() {  // bytes of one position's values
+  return KV == kKvMxfp4 ? kDim / 2 : kDim;
+}
+template <int KV>
+__host__ __device__ constexpr int page_value_bytes() {
+  return kPage * row_bytes<KV>();
+}
+template <int KV>
+__host__ __device__ constexpr int page_bytes() {
+  return page_value_bytes<KV>() + kPage * 4;
+}
 constexpr uint32_t kDevErrLen = 1u, kDevErrPage = 2u, kDevErrBlock = 4u, kDevErrTimeout = 8u, kDevErrReq = 16u;
 constexpr int kLayoutDecode = 0, kLayoutPrefill = 1, kLayoutVarlen = 2;
 
 __device__ __forceinline__ void report(int32_t* dev_err, uint32_t bits) {
   if (dev_err != nullptr) atomicOr(reinterpret_cast<unsigned int*>(dev_err), bits);
+}
+
+// Byte offset of (row r, byte kb) inside a K-major tile of 64-byte rows in the
+// 64-byte swizzle layout (8-row atoms of 512 B; the 16-byte chunk index is
+// XOR-ed with (r / 2) mod 4).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t r, uint32_t kb) {
+  return (r >> 3) * 512u + (r & 7u) * 64u + ((((kb >> 4) ^ ((r >> 1) & 3u)) << 4) | (kb & 15u));
 }
 
 // Byte offset of (row r, byte kb) inside a K-major tile of 128-byte rows in the

@@ -14,6 +14,7 @@ struct PoolArgs {
   const float* w;
   const uint8_t* k_pool;
   int64_t num_pages;
+  int32_t kv_format;  // 0 FP8 pages, 1 MXFP4 pages
   const int32_t* page_table;
   int32_t max_pages;
   int32_t layout;  // 0 decode (row t = request t), 1 prefill (one request), 2 several requests
@@ -90,6 +91,6 @@ int device_sm_count();
 // Tensor map over the value bytes of a paged index-K pool viewed as
 // [num_pages][64 positions][128 bytes], 128-byte swizzle, box of `box_rows`
 // positions of one page.
-cudaError_t make_pool_tmap(CUtensorMap* map, const uint8_t* k_pool, int64_t num_pages, int box_rows);
+cudaError_t make_pool_tmap(CUtensorMap* map, const uint8_t* k_pool, int64_t num_pages, int kv_format, int box_rows);
 
 }  // namespace ci

@@ -22,6 +22,12 @@
 //   warps 4-15  epilogue, three warpgroups: tcgen05.ld of one row's 64 head
 //               columns per position, ReLU + head weights, K scale, length
 //               mask, max over 8 lanes by shuffles, key store.
+// MXFP4 index-K (the use_fp4_cache variant of vLLM sparse_attn_indexer.py):
+// 64-byte packed rows with 64-byte swizzle, the query kept packed, two
+// kind::mxf4 steps of K = 64 per tile; the MMA warp transposes each tile's
+// 128 scale words into shared memory and copies them into tensor memory as
+// the A scale factors (row 32 c + l at column c, lane l); no per-position K
+// scale in the epilogue.
 // Prefill rows share one request's pages, so R = 3 rows ride one MMA
 // (N = 192, two accumulator stages); decode rows each have their own pages,
 // R = 1 (N = 64, six stages) and the three epilogue warpgroups take tiles
@@ -40,10 +46,13 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kTmemCols = 512;
 constexpr int kSfaCol = 384;  // 4 columns: A scale factors (all 1.0)
 constexpr int kSfbCol = 388;  // 8 columns: B scale factors
+constexpr int kSfa4Col = 400;  // MXFP4 K: 4 columns of A scale factors per K stage (32 columns)
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;
 
 struct __align__(1024) Smem {
-  uint8_t kv[kStages][kTileM * kDim];  // A tiles, 1024-aligned
+  // A tiles, 1024-aligned.  MXFP4 tiles take the first 8 KB of a slot and
+  // stage their scale factors for tcgen05.cp at byte 8192 of it.
+  uint8_t kv[kStages][kTileM * kDim];
   uint8_t q[3 * kHeads * kDim];        // B tile (up to 192 rows of 128 B)
   float ks[kScaleSlots][kTileM];       // per-position K scales
   uint64_t k_full[kStages], k_empty[kStages];
@@ -102,17 +111,21 @@ __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
   report(dev_err, kDevErrTimeout);
 }
 
-template <int R>
+template <int R, int KV>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_amax8_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
   constexpr int N = 64 * R;                    // MMA N
   constexpr int kNumAcc = R == 3 ? 2 : 4;      // accumulator stages (power of two)
   constexpr int kEpiPerTile = R == 3 ? 3 : 1;  // epilogue warpgroups consuming each tile
+  constexpr bool kFp4 = KV == kKvMxfp4;
+  constexpr int kPVB = page_value_bytes<KV>(), kPB = page_bytes<KV>();
   // With R = 3 every epilogue warp reads every tile's K scales in order, and
   // the copy into scale slot u + 16 waits for MMA u + 8, which needs all of
   // them past tile u + 6: the slot is free without a barrier of its own.
   // Round-robin warpgroups (R = 1) give no such order, so they release slots.
-  constexpr bool kScaleRelease = R != 3;
+  // MXFP4 scales are read by the MMA warp, in order, before it issues tile u,
+  // so they never need a release either.
+  constexpr bool kScaleRelease = R != 3 && !kFp4;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -263,17 +276,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();  // the previous group is fully consumed
     if (*abort_flag) break;
-    // ---- group set-up: queries widened to e4m3 in the swizzled B tile
-    for (int idx = tid; idx < N * 8; idx += kThreads) {
-      const int n = idx >> 3, c = idx & 7;
-      const int row = grp.first + n / kHeads, head = n % kHeads;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (n / kHeads < grp.count) {
-        const uint2 packed =
-            *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(row) * kHeads + head) * 64 + c * 8);
-        v = widen_fp4x16(packed);
+    // ---- group set-up: the B tile, queries widened to e4m3 (128-byte
+    // swizzled rows) against FP8 K, or kept packed (64-byte swizzled rows)
+    // against MXFP4 K
+    if (kFp4) {
+      for (int idx = tid; idx < N * 4; idx += kThreads) {
+        const int n = idx >> 2, c = idx & 3;
+        const int row = grp.first + n / kHeads, head = n % kHeads;
+        uint2 lo = make_uint2(0, 0), hi = make_uint2(0, 0);
+        if (n / kHeads < grp.count) {
+          const uint2* src =
+              reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(row) * kHeads + head) * 64 + c * 16);
+          lo = src[0];
+          hi = src[1];
+        }
+        *reinterpret_cast<uint4*>(sm.q + sw64_offset(n, c * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
       }
-      *reinterpret_cast<uint4*>(sm.q + sw128_offset(n, c * 16)) = v;
+    } else {
+      for (int idx = tid; idx < N * 8; idx += kThreads) {
+        const int n = idx >> 3, c = idx & 7;
+        const int row = grp.first + n / kHeads, head = n % kHeads;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n / kHeads < grp.count) {
+          const uint2 packed =
+              *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(row) * kHeads + head) * 64 + c * 8);
+          v = widen_fp4x16(packed);
+        }
+        *reinterpret_cast<uint4*>(sm.q + sw128_offset(n, c * 16)) = v;
+      }
     }
     fence_proxy_async_smem();
     if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
@@ -329,14 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t nvalid = (pid[0] >= 0) + (pid[1] >= 0);
-          mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * kPageValueBytes);
+          mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * kPVB);
           mbar_arrive_expect_tx_elect(&sm.s_full[si], nvalid * kPage * 4);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (pid[j] < 0) continue;
-            tma_load_3d_elect(sm.kv[ki] + j * kPageValueBytes, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
-            bulk_load_elect(&sm.ks[si][j * kPage],
-                            a.p.k_pool + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, kPage * 4,
+            tma_load_3d_elect(sm.kv[ki] + j * kPVB, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
+            bulk_load_elect(&sm.ks[si][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPB + kPVB, kPage * 4,
                             &sm.s_full[si]);
           }
           ++issued;
@@ -344,28 +373,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer (whole warp, one lane issues)
+      // FP8 K: four kind::mxf8f6f4 steps of K = 32 (A scale factors 1);
+      // MXFP4 K: two kind::mxf4 steps of K = 64, A scale factors from the
+      // tile's scale words, staged transposed and copied into tensor memory.
       uint64_t bdesc[4];
       uint32_t idesc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q) + 32 * k);
-        idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, N, k, k);
+        bdesc[k] = kFp4 ? sdesc_k64_sw64(smem_u32(sm.q) + 32 * (k & 1)) : sdesc_k128_sw128(smem_u32(sm.q) + 32 * k);
+        idesc[k] = kFp4 ? idesc_mxf4(kTileM, N, 2 * (k & 1), 2 * (k & 1)) : idesc_mxf8f6f4_e4m3(kTileM, N, k, k);
       }
       uint32_t ts = tseq;
       for (int t = off; t < off + take; ++t, ++ts) {
         const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
         const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
-        if (!warp_wait_fast(&sm.k_full[ki], kp, abort_flag) || !warp_wait_fast(&sm.t_empty[ai], ap ^ 1, abort_flag)) {
+        const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+        if (!warp_wait_fast(&sm.k_full[ki], kp, abort_flag) ||
+            (kFp4 && !warp_wait_fast(&sm.s_full[si], sp, abort_flag)) ||
+            !warp_wait_fast(&sm.t_empty[ai], ap ^ 1, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           break;
         }
         tc_fence_after();
         const uint32_t d = tbase + ai * N;
         const uint32_t a0 = smem_u32(sm.kv[ki]);
+        if (kFp4) {
+          // lane l's 16 bytes: the scale words of positions l, 32 + l, 64 + l,
+          // 96 + l (A row 32 c + l <-> column c, lane l, every lane quadrant)
+          const uint32_t* ksw = reinterpret_cast<const uint32_t*>(sm.ks[si]);
+          uint8_t* stage = sm.kv[ki] + 8192;
+          *reinterpret_cast<uint4*>(stage + 16 * lane) =
+              make_uint4(ksw[lane], ksw[32 + lane], ksw[64 + lane], ksw[96 + lane]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t sfa = tbase + kSfa4Col + 4 * ki;
+          tmem_cp_32x128b_x4_elect(sfa, sdesc_rows16(smem_u32(stage)));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol,
-                             tbase + kSfbCol, kk);
+          for (int kk = 0; kk < 2; ++kk)
+            mma_mxf4_elect(d, sdesc_k64_sw64(a0 + 32 * kk), bdesc[kk], idesc[kk], sfa, tbase + kSfbCol, kk);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol,
+                               tbase + kSfbCol, kk);
+        }
         mma_commit_elect(&sm.k_empty[ki]);
         mma_commit_elect(&sm.t_full[ai]);
       }
@@ -400,11 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.t_empty[ai]);
         const float score = head_reduce_finish(part);
-        if (!warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
-          if (lane == 0) set_abort(sm, a.p.dev_err);
-          break;
+        float kscale = 1.0f;  // MXFP4: the scales are inside the MMA
+        if (!kFp4) {
+          if (!warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
+            if (lane == 0) set_abort(sm, a.p.dev_err);
+            break;
+          }
+          kscale = sm.ks[si][p];
         }
-        const float kscale = sm.ks[si][p];
         if (kScaleRelease) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.s_empty[si]);
@@ -445,21 +499,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <int R, int KV>
+cudaError_t launch_one(const CUtensorMap& tmap, const DenseArgs& a, int smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(dense_amax8_kernel<R, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dense_amax8_kernel<R, KV><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dense_amax8(const DenseArgs& a, cudaStream_t stream) {
   CUtensorMap tmap;
-  cudaError_t e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, kPage);
+  cudaError_t e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, a.p.kv_format, kPage);
   if (e != cudaSuccess) return e;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
-  if (a.p.layout != kLayoutDecode) {
-    e = cudaFuncSetAttribute(dense_amax8_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    dense_amax8_kernel<3><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
-  } else {
-    e = cudaFuncSetAttribute(dense_amax8_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    dense_amax8_kernel<1><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
-  }
-  return cudaGetLastError();
+  const bool prefill = a.p.layout != kLayoutDecode;
+  if (a.p.kv_format == kKvMxfp4)
+    return prefill ? launch_one<3, kKvMxfp4>(tmap, a, smem, stream) : launch_one<1, kKvMxfp4>(tmap, a, smem, stream);
+  return prefill ? launch_one<3, kKvFp8>(tmap, a, smem, stream) : launch_one<1, kKvFp8>(tmap, a, smem, stream);
 }
 
 }  // namespace ci

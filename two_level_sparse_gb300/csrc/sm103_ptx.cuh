@@ -121,6 +121,9 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -230,6 +233,19 @@ __device__ __forceinline__ uint64_t sdesc_k128_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// The same for rows of 64 bytes (K = 128 packed e2m1 codes) in the 64-byte
+// swizzled layout: 8-row atoms of 512 B, the 16-byte chunk index XOR-ed with
+// (row / 2) mod 4.
+__device__ __forceinline__ uint64_t sdesc_k64_sw64(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;           // leading byte offset (unused for this layout)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;    // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;           // version
+  d |= static_cast<uint64_t>(4u) << 61;           // swizzle 64B
+  return d;
+}
+
 // Instruction descriptor, kind::f8f6f4 (no block scale), fp32 accumulate,
 // both operands E4M3 and K-major.
 __host__ __device__ constexpr uint32_t idesc_f8f6f4_e4m3(uint32_t M, uint32_t N) {
@@ -244,6 +260,14 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4_e4m3(uint32_t M, uint32_t N)
 __host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3(uint32_t M, uint32_t N, uint32_t sfa_id,
                                                           uint32_t sfb_id) {
   return ((sfb_id & 3u) << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         ((sfa_id & 3u) << 29);
+}
+
+// Instruction descriptor, kind::mxf4 (packed e2m1 x e2m1, UE8M0 scale factors
+// per 32 elements, K = 64 per instruction), both operands K-major; sfa_id /
+// sfb_id (0 or 2) select the two bytes of the 32-bit scale-factor column used.
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {
+  return ((sfb_id & 3u) << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          ((sfa_id & 3u) << 29);
 }
 
@@ -302,6 +326,15 @@ __device__ __forceinline__ void mma_mxf8f6f4_elect(uint32_t d_tmem, uint64_t ade
   asm volatile(
       "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf4_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

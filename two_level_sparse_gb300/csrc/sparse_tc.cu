@@ -15,19 +15,24 @@
 //               factors into tensor memory, then per 128-position tile four
 //               tcgen05.mma kind::mxf8f6f4 block_scale (M = 128 gathered
 //               positions, N = 64 heads, K = 32 each) into one of three
-//               accumulator stages;
-//   warps 1-3   gather a tile's 16 candidate blocks (each 1 KB of contiguous K
-//               in its page) into a 128-byte-swizzled MMA tile of a 9-deep
-//               ring: warp 1 with 8-row tensor-map loads for 6 of them,
-//               warps 2-3 with 16-byte cp.async for the other 10 (each path
-//               alone is capped well below what both reach together);
+//               accumulator stages -- or, for MXFP4 K, a tcgen05.cp of the
+//               tile's K scale factors and two kind::mxf4 steps of K = 64;
+//   warps 1-3   gather a tile's 16 candidate blocks (each contiguous K in its
+//               page: 1 KB FP8, 512 B MXFP4) into a swizzled MMA tile of a
+//               9-deep ring: warp 1 with 8-row tensor-map loads for 6 (MXFP4:
+//               8) of them, warps 2-3 with 16-byte cp.async for the others
+//               (each path alone is capped well below what both reach
+//               together); for MXFP4 warps 2-3 also stage the 128 positions'
+//               scale words for the MMA warp's tcgen05.cp;
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
 //               then, two rows ahead, the page of every candidate block, the
-//               query widened from e2m1 to e4m3 and its scale factors staged;
+//               query (widened from e2m1 to e4m3 against FP8 K, packed against
+//               MXFP4 K) and its scale factors staged;
 //   warps 8-15  two scoring warpgroups, tiles alternating: each thread loads
-//               its position's K scale straight from the pool, then the same
-//               epilogue arithmetic as the dense pass and one order-preserving
-//               key per candidate stored as one tensor-memory column per tile.
+//               its position's FP8 K scale straight from the pool, then the
+//               same epilogue arithmetic as the dense pass and one
+//               order-preserving key per candidate stored as one
+//               tensor-memory column per tile.
 // Scores never leave the chip, and the shared memory they would need goes to
 // the gather ring instead.
 #include "ci_common.cuh"
@@ -42,11 +47,18 @@ constexpr int kNumAcc = 3;
 constexpr int kSfaCol = 192;      // 4 columns of A scale factors (all 1.0)
 constexpr int kSfbCol = 196;      // two buffers of 4 columns of B scale factors
 constexpr int kScoreCol = 208;    // two buffers of kMaxTiles score columns
+constexpr int kSfa4Col = 480;     // MXFP4 K: 4 columns of A scale factors per accumulator stage
 constexpr int kBlocksPerTile = kTileM / kBlock;  // 16
 constexpr int kMaxBlocks = 2176;                 // >= topk + 1 for every supported topk
 constexpr int kMaxTiles = kMaxBlocks / kBlocksPerTile;  // 136
 constexpr int kGatherWarp0 = 1, kGatherWarps = 3;  // warp 1 tensor-map loads, warps 2-3 cp.async
-constexpr int kTmaBlocks = 6;  // blocks of a tile fetched by tensor-map loads (the rest by cp.async)
+// Blocks of a tile fetched by tensor-map loads, the rest by cp.async: the
+// split that balances the two paths (measured: FP8 1 KB blocks 6, MXFP4
+// 512-byte blocks 8).
+template <int KV>
+__host__ __device__ constexpr int tma_blocks() {
+  return KV == kKvMxfp4 ? 8 : 6;
+}
 constexpr int kTopkWarp0 = 4, kTopkThreads = 128, kTopkBar = 2;  // also the next-row prep
 constexpr int kPrepThreads = kTopkThreads;
 constexpr int kScoreWarp0 = 8;
@@ -62,7 +74,9 @@ struct TopkShared {
 };
 
 struct __align__(1024) Smem {
-  uint8_t kv[kStages][kTileM * kDim];  // gathered A tiles (1024-aligned)
+  // gathered A tiles (1024-aligned); MXFP4 tiles take the first 8 KB of a slot
+  // and stage their scale factors for tcgen05.cp at byte 8192 of it
+  uint8_t kv[kStages][kTileM * kDim];
   uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered
   uint8_t sf[2][512];                  // query scale factors staged for tcgen05.cp
   // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
@@ -147,16 +161,28 @@ struct Ring {
 // swizzled B tile, its scale factors staged for tcgen05.cp, and for every
 // candidate block its physical page, its slot in the page and how many of its
 // positions lie below L.
+template <int KV>
 __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
                                          volatile int* abort_flag) {
   const int b = ri & 1;
   const uint32_t ph = (ri >> 1) & 1;
   bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
-  for (int idx = pid_t; ok && idx < kHeads * 8; idx += kPrepThreads) {
-    const int head = idx >> 3, c = idx & 7;
-    const uint2 packed =
-        *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(r.row) * kHeads + head) * 64 + c * 8);
-    *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(head, c * 16)) = widen_fp4x16(packed);
+  if (KV == kKvMxfp4) {
+    // packed e2m1 rows of 64 bytes, 64-byte swizzle
+    for (int idx = pid_t; ok && idx < kHeads * 4; idx += kPrepThreads) {
+      const int head = idx >> 2, c = idx & 3;
+      const uint2* src =
+          reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(r.row) * kHeads + head) * 64 + c * 16);
+      const uint2 lo = src[0], hi = src[1];
+      *reinterpret_cast<uint4*>(sm.q[b] + sw64_offset(head, c * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  } else {
+    for (int idx = pid_t; ok && idx < kHeads * 8; idx += kPrepThreads) {
+      const int head = idx >> 3, c = idx & 7;
+      const uint2 packed =
+          *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(r.row) * kHeads + head) * 64 + c * 8);
+      *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(head, c * 16)) = widen_fp4x16(packed);
+    }
   }
   if (ok && pid_t < 32) {
     // lane l of the scale-factor columns: heads l and 32 + l, byte j = K block j
@@ -435,8 +461,13 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   }
 }
 
+template <int KV>
 __global__ void __launch_bounds__(kThreads, 1)
     select_kernel(const __grid_constant__ CUtensorMap tmap, const SelectArgs a) {
+  constexpr bool kFp4 = KV == kKvMxfp4;
+  constexpr int kBlockBytes = kBlock * row_bytes<KV>();  // one candidate block's values: 1 KB or 512 B
+  constexpr int kPVB = page_value_bytes<KV>(), kPB = page_bytes<KV>();
+  constexpr int kTmaBlocks = tma_blocks<KV>();
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -503,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t idesc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        bdesc[k] = sdesc_k128_sw128(smem_u32(sm.q[b]) + 32 * k);
-        idesc[k] = idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
+        bdesc[k] = kFp4 ? sdesc_k64_sw64(smem_u32(sm.q[b]) + 32 * (k & 1)) : sdesc_k128_sw128(smem_u32(sm.q[b]) + 32 * k);
+        idesc[k] = kFp4 ? idesc_mxf4(kTileM, kHeads, 2 * (k & 1), 2 * (k & 1)) : idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
       }
       for (int t = 0; t < r.ntiles; ++t) {
         if (!warp_wait_fast(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
@@ -517,9 +548,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tbase + ar.idx * kHeads;
         const uint32_t a0 = smem_u32(sm.kv[kr.idx]);
+        if (kFp4) {
+          // the tile's A scale factors (staged transposed by the gather warps),
+          // one slot per accumulator stage: the MMAs that read a slot finished
+          // before t_empty let this stage be reused
+          const uint32_t sfa = tbase + kSfa4Col + 4 * ar.idx;
+          tmem_cp_32x128b_x4_elect(sfa, sdesc_rows16(a0 + 8192));
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * k), bdesc[k], idesc[k], tbase + kSfaCol, sfb, k);
+          for (int k = 0; k < 2; ++k)
+            mma_mxf4_elect(d, sdesc_k64_sw64(a0 + 32 * k), bdesc[k], idesc[k], sfa, sfb, k);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * k), bdesc[k], idesc[k], tbase + kSfaCol, sfb, k);
+        }
         mma_commit_elect(&sm.k_empty[kr.idx]);
         mma_commit_elect(&sm.t_full[ar.idx]);
         kr.next(kStages);
@@ -558,27 +600,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = row_base + lane;
           const int v = lane < kTmaBlocks && slot < r.nv ? info[slot] : -1;
           const uint32_t live = __ballot_sync(0xffffffffu, v >= 0);
-          mbar_arrive_expect_tx_elect(&sm.tk_full[kr.idx], __popc(live) * (kBlock * kDim));
+          mbar_arrive_expect_tx_elect(&sm.tk_full[kr.idx], __popc(live) * kBlockBytes);
 #pragma unroll
           for (int blk = 0; blk < kTmaBlocks; ++blk) {
             const int vb = __shfl_sync(0xffffffffu, v, blk);
             if (vb >= 0)
-              tma_load_3d_elect(dst + blk * (kBlock * kDim), &tmap, 0, ((vb >> 4) & 7) * kBlock, vb >> 7,
+              tma_load_3d_elect(dst + blk * kBlockBytes, &tmap, 0, ((vb >> 4) & 7) * kBlock, vb >> 7,
                                 &sm.tk_full[kr.idx]);
           }
           ++issued;
         } else {
-          // block blk: 1 KB contiguous in its page -> one 8-row swizzle atom;
-          // lane l copies 16-byte chunks l and l + 32 (rows l / 8 and 4 + l / 8)
+          // block blk: contiguous in its page -> one 8-row swizzle atom;
+          // FP8 (1 KB): lane l copies 16-byte chunks l and l + 32 (rows l / 8
+          // and 4 + l / 8); MXFP4 (512 B): lane l copies chunk l (row l / 4)
 #pragma unroll 2
           for (int blk = kTmaBlocks + gw - 1; blk < kBlocksPerTile; blk += kGatherWarps - 1) {
             const int slot = row_base + blk;
             const int v = slot < r.nv ? info[slot] : -1;
             if (v >= 0) {
-              const uint8_t* src = a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes +
-                                   ((v >> 4) & 7) * (kBlock * kDim) + lane * 16;
-              cp_async16(dst + blk * (kBlock * kDim) + dst0, src);
-              cp_async16(dst + blk * (kBlock * kDim) + dst1, src + 512);
+              const uint8_t* src =
+                  a.p.k_pool + static_cast<int64_t>(v >> 7) * kPB + ((v >> 4) & 7) * kBlockBytes + lane * 16;
+              if (kFp4) {
+                cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
+              } else {
+                cp_async16(dst + blk * kBlockBytes + dst0, src);
+                cp_async16(dst + blk * kBlockBytes + dst1, src + 512);
+              }
+            }
+          }
+          if (kFp4) {
+            // the scale words of all 128 positions, staged for tcgen05.cp:
+            // position p = 32 c + l goes to byte 16 l + 4 c
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int p = (gw - 1) * 64 + 32 * j + lane;
+              const int slot = row_base + (p >> 3);
+              const int v = slot < r.nv ? info[slot] : -1;
+              if (v >= 0)
+                cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
+                          a.p.k_pool + static_cast<int64_t>(v >> 7) * kPB + kPVB + 4 * (((v >> 4) & 7) * kBlock + (p & 7)));
             }
           }
           cp_async_arrive_noinc(&sm.k_full[kr.idx]);
@@ -603,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // across the four warps before anyone acts on it
     auto prep = [&](int pi) -> bool {
       const int prow = blockIdx.x + pi * gridDim.x;
-      const bool mine = prow >= rows || prep_row(sm, a, row_info(a, prow, false), pi, kt, abort_flag);
+      const bool mine = prow >= rows || prep_row<KV>(sm, a, row_info(a, prow, false), pi, kt, abort_flag);
       if (lane == 0) sm.prep_ok[warp & 3] = mine ? 1 : 0;
       named_sync(kTopkBar, kTopkThreads);
       const bool all = sm.prep_ok[0] && sm.prep_ok[1] && sm.prep_ok[2] && sm.prep_ok[3];
@@ -673,10 +733,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int v = slot < r.nv ? sm.info[b][slot] : -1;
           const bool valid = v >= 0 && (p & 7) < (v & 15);
           // this position's K scale, fetched now and used after the head sum
-          float kscale = 0.0f;
-          if (valid)
-            kscale = __ldg(reinterpret_cast<const float*>(a.p.k_pool + static_cast<int64_t>(v >> 7) * kPageBytes +
-                                                          kPageValueBytes) +
+          // (MXFP4: 1, the scales are inside the MMA)
+          float kscale = kFp4 ? 1.0f : 0.0f;
+          if (!kFp4 && valid)
+            kscale = __ldg(reinterpret_cast<const float*>(a.p.k_pool + static_cast<int64_t>(v >> 7) * kPB + kPVB) +
                            ((v >> 4) & 7) * kBlock + (p & 7));
           if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
             ok = false;
@@ -731,17 +791,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t select_smem_bytes(int) { return sizeof(Smem) + 1024; }
 
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
-  if (a.p.rows == 0) return cudaSuccess;
+template <int KV>
+cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
   const int smem = static_cast<int>(select_smem_bytes(a.max_blocks));
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   CUtensorMap tmap;
-  e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, kBlock);
+  e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, KV, kBlock);
   if (e != cudaSuccess) return e;
   const int grid = min(device_sm_count(), a.p.rows);
-  select_kernel<<<grid, kThreads, smem, stream>>>(tmap, a);
+  select_kernel<KV><<<grid, kThreads, smem, stream>>>(tmap, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
+  if (a.p.rows == 0) return cudaSuccess;
+  return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4>(a, stream) : launch_select_kv<kKvFp8>(a, stream);
 }
 
 }  // namespace ci

@@ -16,7 +16,11 @@ Operand formats (the ones the DeepSeek-V4.1 indexer pages describe):
   endian fp32 scales (8448 bytes).  Pages sit in a pool in a random physical
   order behind an int32 page table ``page_table[num_req, max_pages]``
   (vLLM ``sparse_attn_indexer.py``, K-gather workspace: ``(T, head_dim)`` fp8
-  values + ``(T, 4)`` bytes of fp32 scale per position).
+  values + ``(T, 4)`` bytes of fp32 scale per position);
+* index-K, MXFP4 variant (the same file's ``use_fp4_cache`` path: ``head_dim
+  / 2`` packed bytes and ``head_dim / 32`` ue8m0 scales per position): a page
+  is ``64*64`` bytes of packed e2m1 codes followed by one 32-bit word per
+  position whose byte ``j`` scales elements ``32j .. 32j + 31`` (4352 bytes).
 
 Workloads (one source layer + four consumer layers, each with its own q, w and
 K pool, one shared page table):
@@ -38,6 +42,9 @@ BLOCK = 8
 PAGE = 64
 PAGE_VALUE_BYTES = PAGE * D
 PAGE_BYTES = PAGE * D + PAGE * 4
+KV_FP8, KV_MXFP4 = 0, 1
+PAGE_VALUE_BYTES_MXFP4 = PAGE * D // 2
+PAGE_BYTES_MXFP4 = PAGE_VALUE_BYTES_MXFP4 + PAGE * 4
 LAYOUT_DECODE = 0
 LAYOUT_PREFILL = 1
 LAYOUT_VARLEN = 2  # a prefill chunk of several requests: rows req_start[r] .. req_start[r + 1] - 1 are request r
@@ -84,6 +91,10 @@ class Workload:
     def num_pages(self) -> int:
         return int(self.layers[0].k_pool.shape[0])
 
+    @property
+    def kv(self) -> int:
+        return KV_MXFP4 if int(self.layers[0].k_pool.shape[1]) == PAGE_BYTES_MXFP4 else KV_FP8
+
     def to(self, device) -> "Workload":
         mv = lambda t: t.to(device)
         return Workload(
@@ -112,12 +123,27 @@ def _k_pages(num_pages: int, gen: torch.Generator, device, chunk_pages: int = 20
     return pool
 
 
-def _layer(rows: int, num_pages: int, gen: torch.Generator, device) -> Layer:
+def _k_pages_mxfp4(num_pages: int, gen: torch.Generator, device, chunk_pages: int = 4096) -> torch.Tensor:
+    """MXFP4 pages: uniformly random e2m1 codes (both nibbles of every byte)
+    and ue8m0 scales with exponents uniform in [-4, 0] (codes 123..127), the
+    same distribution as the queries."""
+    pool = torch.empty(num_pages, PAGE_BYTES_MXFP4, dtype=torch.uint8, device=device)
+    for p0 in range(0, num_pages, chunk_pages):
+        n = min(chunk_pages, num_pages - p0)
+        pool[p0 : p0 + n, :PAGE_VALUE_BYTES_MXFP4] = torch.randint(
+            0, 256, (n, PAGE_VALUE_BYTES_MXFP4), generator=gen, device=device, dtype=torch.uint8)
+        pool[p0 : p0 + n, PAGE_VALUE_BYTES_MXFP4:] = torch.randint(
+            123, 128, (n, PAGE * 4), generator=gen, device=device, dtype=torch.uint8)
+    return pool
+
+
+def _layer(rows: int, num_pages: int, gen: torch.Generator, device, kv: int = KV_FP8) -> Layer:
     q_fp4 = torch.randint(0, 256, (rows, H, D // 2), generator=gen, device=device, dtype=torch.uint8)
     # ue8m0 exponent uniform in [-4, 0]: codes 123..127
     q_sf = torch.randint(123, 128, (rows, H, D // 32), generator=gen, device=device, dtype=torch.uint8)
     w = torch.randn(rows, H, generator=gen, device=device) * (1.0 / math.sqrt(H))
-    return Layer(q_fp4, q_sf, w.float(), _k_pages(num_pages, gen, device))
+    pool = _k_pages_mxfp4(num_pages, gen, device) if kv == KV_MXFP4 else _k_pages(num_pages, gen, device)
+    return Layer(q_fp4, q_sf, w.float(), pool)
 
 
 def _duplicate_blocks(layer: Layer, page_table: torch.Tensor, seq_len: torch.Tensor, req_rows,
@@ -125,6 +151,8 @@ def _duplicate_blocks(layer: Layer, page_table: torch.Tensor, seq_len: torch.Ten
     """Overwrite ``frac`` of each request's full, non-newest blocks with a byte
     copy (values and scales) of another such block of the same request."""
     pool = layer.k_pool
+    rb = D // 2 if int(pool.shape[1]) == PAGE_BYTES_MXFP4 else D  # value bytes per position
+    pvb = PAGE * rb
     for r, L in req_rows:
         nb = (L + BLOCK - 1) // BLOCK
         nfull = nb - 1  # every block but the newest is full
@@ -138,14 +166,12 @@ def _duplicate_blocks(layer: Layer, page_table: torch.Tensor, seq_len: torch.Ten
                 src += 1
             sp, so = int(page_table[r, src // 8]), (src % 8) * BLOCK
             dp, do = int(page_table[r, dst // 8]), (dst % 8) * BLOCK
-            pool[dp, do * D : (do + BLOCK) * D] = pool[sp, so * D : (so + BLOCK) * D]
-            pool[dp, PAGE_VALUE_BYTES + do * 4 : PAGE_VALUE_BYTES + (do + BLOCK) * 4] = pool[
-                sp, PAGE_VALUE_BYTES + so * 4 : PAGE_VALUE_BYTES + (so + BLOCK) * 4
-            ]
+            pool[dp, do * rb : (do + BLOCK) * rb] = pool[sp, so * rb : (so + BLOCK) * rb]
+            pool[dp, pvb + do * 4 : pvb + (do + BLOCK) * 4] = pool[sp, pvb + so * 4 : pvb + (so + BLOCK) * 4]
 
 
 def make_workload(name: str, layout: int, seq_len, topk_blocks: int, seed: int, layers: int = 5,
-                  dup_frac: float = 0.0, device="cpu", topk: int = TOPK_POSITIONS) -> Workload:
+                  dup_frac: float = 0.0, device="cpu", topk: int = TOPK_POSITIONS, kv: int = KV_FP8) -> Workload:
     """Build one workload from explicit per-row lengths."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
@@ -171,7 +197,7 @@ def make_workload(name: str, layout: int, seq_len, topk_blocks: int, seed: int, 
             page_table = torch.full((1, 1), -1, dtype=torch.int32)
         req_rows = [(0, max_len)]
     num_pages = max(num_pages, 1)
-    ls = [_layer(rows, num_pages, gen, device) for _ in range(layers)]
+    ls = [_layer(rows, num_pages, gen, device, kv) for _ in range(layers)]
     if dup_frac > 0:
         cpu_gen = torch.Generator().manual_seed(seed + 104729)
         for l in ls:
@@ -183,7 +209,7 @@ def make_workload(name: str, layout: int, seq_len, topk_blocks: int, seed: int, 
 
 
 def make_varlen_workload(name: str, prefixes, rows_per_req, topk_blocks: int, seed: int, layers: int = 5,
-                         device="cpu", topk: int = TOPK_POSITIONS) -> Workload:
+                         device="cpu", topk: int = TOPK_POSITIONS, kv: int = KV_FP8) -> Workload:
     """A prefill chunk of several requests: request r contributes
     rows_per_req[r] causal rows after a prefix of prefixes[r] compressed
     positions (row i of the request reaches prefixes[r] + i + 1 positions).
@@ -206,7 +232,7 @@ def make_varlen_workload(name: str, prefixes, rows_per_req, topk_blocks: int, se
     for r, n in enumerate(pages_per):
         page_table[r, :n] = perm[off : off + n].to(torch.int32)
         off += n
-    ls = [_layer(rows, num_pages, gen, device) for _ in range(layers)]
+    ls = [_layer(rows, num_pages, gen, device, kv) for _ in range(layers)]
     return Workload(name, LAYOUT_VARLEN, seq_len.to(device), page_table.to(device), ls, topk_blocks, topk,
                     torch.as_tensor(starts, dtype=torch.int32).to(device))
 
@@ -261,9 +287,11 @@ CONFIG_LAYOUT = {0: LAYOUT_DECODE, 1: LAYOUT_DECODE, 2: LAYOUT_DECODE, 3: LAYOUT
 CONFIG_TOPK_BLOCKS = {0: 128, 1: 2048, 2: 2048, 3: 2048, 4: 2048}
 
 
-def config_workload(cid: int, device="cpu", layers: int = 5) -> Workload:
+def config_workload(cid: int, device="cpu", layers: int = 5, kv: int = KV_FP8) -> Workload:
+    """Standard workload ``cid``; ``kv = KV_MXFP4`` draws MXFP4 pools instead
+    of FP8 ones (same lengths, queries and weights; name suffixed)."""
     return make_workload(
-        CONFIG_NAMES[cid],
+        CONFIG_NAMES[cid] + ("_mxfp4" if kv == KV_MXFP4 else ""),
         CONFIG_LAYOUT[cid],
         config_lengths(cid),
         CONFIG_TOPK_BLOCKS[cid],
@@ -271,4 +299,5 @@ def config_workload(cid: int, device="cpu", layers: int = 5) -> Workload:
         layers=layers,
         dup_frac=0.05 if cid == 0 else 0.0,
         device=device,
+        kv=kv,
     )
