@@ -350,6 +350,44 @@ def measure_mxfp4(steps, stream, flush, world, peaks):
     return line
 
 
+QPROD_TOKENS = 16384
+
+
+def measure_qprod(steps, stream, flush, peaks):
+    """The query producer on a 16384-token chunk (RoPE, MXFP4 quantization,
+    weight scaling), inputs resident, L2 flushed before every launch."""
+    from two_level_sparse_gb300 import ci
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    t, max_pos = QPROD_TOKENS, 262144
+    q = torch.randn(t, 64, 128, generator=g, device="cuda").to(torch.bfloat16)
+    ang = torch.rand(max_pos, 32, generator=g, device="cuda") * 6.2831853
+    cos_sin = torch.cat([torch.cos(ang), torch.sin(ang)], 1).contiguous()
+    pos = torch.arange(max_pos - t, max_pos, dtype=torch.int32, device="cuda")
+    w = torch.randn(t, 64, generator=g, device="cuda")
+    q_fp4 = torch.empty(t, 64, 64, dtype=torch.uint8, device="cuda")
+    q_sf = torch.empty(t, 64, 4, dtype=torch.uint8, device="cuda")
+    w_out = torch.empty(t, 64, dtype=torch.float32, device="cuda")
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ci.ci_q_rope_quant(pos, q, cos_sin, w, 0.0625, 0.125, True, ci.Q_MXFP4, q_fp4, q_sf, w_out, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                ms.append(e0.elapsed_time(e1))
+    m = statistics.mean(ms)
+    moved = t * 64 * (256 + 4 + 64 + 4 + 4) + t * (4 + 256)  # q, w in; codes, scales, w out; positions, cos/sin rows
+    return {"metric": "query producer ms per 16K-token chunk (RoPE + MXFP4 + weights)",
+            "workload": f"qprod_{t}tokens_64heads_neox", "value": m, "unit": "ms",
+            "roofline": {"bound": "hbm", "achieved": moved / (m * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": moved / (m * 1e-3) / 1e9 / peaks["hbm_gbs"], "bytes": moved}}
+
+
 VARLEN_TAIL_ROWS = 512  # tail rows kept per request by the prefill_tail timing
 
 
@@ -474,6 +512,8 @@ def main():
         secondary.append(measure_varlen(max(3, args.steps // 2), stream, flush, world))
         torch.cuda.empty_cache()
         secondary.append(measure_mxfp4(max(3, args.steps // 2), stream, flush, world, peaks))
+        torch.cuda.empty_cache()
+        secondary.append(measure_qprod(max(3, args.steps // 2), stream, flush, peaks))
         torch.cuda.empty_cache()
 
     cpu_ms, cpu_rows, cpu_threads, nrows = (None, 0, 0, 0)

@@ -19,6 +19,9 @@
  *                            reading the keys once;
  *     ci_prefill_tail        the published table of the last rows of each
  *                            request of a multi-request chunk;
+ *   before level one, once per layer:
+ *     ci_q_rope_quant        the query producer: RoPE, quantization to the
+ *                            indexer's query format, head-weight scaling;
  *   level two, once per layer (the source itself and each consumer):
  *     ci_select_sparse       scores only the positions inside a row's
  *                            published blocks and returns its top-k positions,
@@ -114,6 +117,7 @@ enum ci_status {
 
 enum ci_layout { CI_LAYOUT_DECODE = 0, CI_LAYOUT_PREFILL = 1, CI_LAYOUT_VARLEN = 2 };
 enum ci_kv_format { CI_KV_FP8 = 0, CI_KV_MXFP4 = 1 };
+enum ci_q_format { CI_Q_MXFP4 = 0, CI_Q_FP8 = 1 };
 
 /* Bits OR-ed into *dev_err by the kernels. */
 #define CI_DEVERR_LEN 1u     /* seq_len[t] < 0 or > max_len */
@@ -121,6 +125,7 @@ enum ci_kv_format { CI_KV_FP8 = 0, CI_KV_MXFP4 = 1 };
 #define CI_DEVERR_BLOCK 4u   /* candidate block id outside [0, ceil(L_t/8)) or nvalid out of range */
 #define CI_DEVERR_TIMEOUT 8u /* an on-chip pipeline wait gave up (should never happen) */
 #define CI_DEVERR_REQ 16u    /* req_row_start is not a partition of the rows (CI_LAYOUT_VARLEN) */
+#define CI_DEVERR_POS 32u    /* a RoPE position outside [0, max_pos) (ci_q_rope_quant) */
 
 /*
  * Level one, scoring: block keys of the source layer.
@@ -232,6 +237,36 @@ CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const flo
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
                      int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
                      void* stream);
+
+/*
+ * The query producer (vLLM indexer.py page, rope_quant_q; the
+ * fused_indexer_q_rope_quant kernel of sparse_attn_indexer.py).
+ *
+ * For every token t and head h of q (bf16 bit patterns, [tokens][64][128]):
+ * the pairs (x0, x1) of dims (i, 32 + i) (is_neox != 0) or (2i, 2i + 1)
+ * (is_neox == 0), i < 32, become r0 = x0 c - x1 s and r1 = x1 c + x0 s with
+ * c = cos_sin[p][i], s = cos_sin[p][32 + i], p = positions[t], computed in
+ * fp32 with one rounding per operation and then rounded to bf16; dims 64..127
+ * pass unrotated.  With e(v, m) = ceil(log2(max(v, 1e-10) * (1/m))) taken
+ * exactly from the bits of the fp32 product:
+ *   CI_Q_MXFP4  per block of 32 dims, e = e(amax of the block, 6): q_out
+ *               [tokens][64][64] holds the e2m1 codes of x * 2^-e (nearest,
+ *               ties to even, saturating at 6; element 2i in the low nibble),
+ *               q_sf [tokens][64][4] the codes e + 127, and w_out[t][h] =
+ *               (w[t][h] * softmax_scale) * head_scale: the indexer's inputs.
+ *   CI_Q_FP8    one e = e(amax of the head, 448) per head: q_out
+ *               [tokens][64][128] holds e4m3(clamp(x * 2^-e, -448, 448))
+ *               (nearest even), q_sf is unused (may be NULL), and w_out =
+ *               ((w * 2^e) * softmax_scale) * head_scale, the scale folded into
+ *               the weight as the pages print it.
+ * A position outside [0, max_pos) sets CI_DEVERR_POS and the token's heads are
+ * produced from zeros.  positions int32 [tokens]; cos_sin float [max_pos][64];
+ * w, w_out float [tokens][64]; all device memory; q_sf 4-byte aligned.
+ */
+CI_API int ci_q_rope_quant(const int32_t* positions, const uint16_t* q, const float* cos_sin, int32_t max_pos,
+                           const float* w, float softmax_scale, float head_scale, int32_t is_neox, int32_t tokens,
+                           int32_t out_format, uint8_t* q_out, uint8_t* q_sf, float* w_out, int32_t* dev_err,
+                           void* stream);
 
 /* Human-readable name of a ci_status code (static storage). */
 CI_API const char* ci_strerror(int status);

@@ -29,8 +29,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(
-        ["ci_prefill_tail", "ci_publish_blocks", "ci_publish_blocks2", "ci_score_dense_amax8", "ci_select_sparse",
-         "ci_strerror", "ci_version"])
+        ["ci_prefill_tail", "ci_publish_blocks", "ci_publish_blocks2", "ci_q_rope_quant", "ci_score_dense_amax8",
+         "ci_select_sparse", "ci_strerror", "ci_version"])
 
 
 def test_library_exports_every_declared_symbol(ci):
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(ci):
 
 
 def test_status_names(ci):
-    assert ci.version() == 200
+    assert ci.version() == 201
     assert ci.strerror(0) == "ok"
     for code in ci.CI_ERR:
         assert ci.strerror(code) != "unknown status"
@@ -129,6 +129,27 @@ def test_prefill_tail_host_checks(ci):
     bad = list(ok_args)
     bad[9] = N  # capacity but no output table
     assert f(*bad) == -1
+
+
+def test_q_rope_quant_host_checks(ci):
+    f = ci.lib.ci_q_rope_quant
+    ok_args = [P, P, P, 100, P, 0.125, 0.125, 1, 4, 0, P, P, P, N, N]
+    assert f(*ok_args[:8], 0, *ok_args[9:]) == 0  # no tokens
+    bad = list(ok_args)
+    bad[9] = 2  # unknown output format
+    assert f(*bad) == -5
+    bad = list(ok_args)
+    bad[11] = N  # MXFP4 needs the scale output
+    assert f(*bad) == -1
+    bad = list(ok_args)
+    bad[1] = N
+    assert f(*bad) == -1
+    bad = list(ok_args)
+    bad[11] = ctypes.c_void_p(0x1002)  # scale output not 4-byte aligned
+    assert f(*bad) == -3
+    bad = list(ok_args)
+    bad[8] = -1
+    assert f(*bad) == -2
 
 
 def test_select_host_checks(ci):

@@ -5,6 +5,8 @@ run at full size in the same launch configuration the benchmark uses and are
 checked on sampled rows (every output of a sampled row: keys, published
 blocks, the source's own top-512 and the four consumers' top-512).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -472,3 +474,75 @@ def test_mxfp4_full_size_config_sampled_rows(ci, cid):
     out = step.outputs_numpy()
     sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
     assert_ok(compare.check_step(sub, sub_out))
+
+
+# ----------------------------------------------------------------------------- query producer
+def _producer_inputs(tokens, seed, max_pos=4096):
+    from oracle import q_producer as QP
+
+    g = torch.Generator().manual_seed(seed)
+    mag = 10.0 ** (torch.rand(tokens, 64, 1, generator=g) * 6 - 3)
+    q = (torch.randn(tokens, 64, 128, generator=g) * mag).to(torch.bfloat16)
+    q[0, 0] = 0  # an all-zero head
+    q[0, 1, 5] = -0.0
+    ang = torch.rand(max_pos, 32, generator=g, dtype=torch.float64) * 2 * math.pi
+    cos_sin = torch.cat([torch.cos(ang), torch.sin(ang)], 1).float()
+    pos = torch.randint(0, max_pos, (tokens,), generator=g, dtype=torch.int32)
+    w = torch.randn(tokens, 64, generator=g) * 0.125
+    return pos, q, cos_sin, w, QP
+
+
+def _run_producer(ci, pos, q, cos_sin, w, neox, fmt, dev_err=None):
+    t = q.shape[0]
+    d = "cuda"
+    q_out = torch.empty(t, 64, 128 if fmt == ci.Q_FP8 else 64, dtype=torch.uint8, device=d)
+    q_sf = torch.empty(t, 64, 4, dtype=torch.uint8, device=d) if fmt == ci.Q_MXFP4 else None
+    w_out = torch.empty(t, 64, dtype=torch.float32, device=d)
+    ci.ci_q_rope_quant(pos.to(d), q.to(d), cos_sin.to(d), w.to(d), 0.0625, 0.125, neox, fmt, q_out, q_sf, w_out,
+                       dev_err=dev_err)
+    torch.cuda.synchronize()
+    return q_out.cpu().numpy(), None if q_sf is None else q_sf.cpu().numpy(), w_out.cpu().numpy()
+
+
+@needs_cuda
+@pytest.mark.parametrize("neox", [True, False])
+@pytest.mark.parametrize("fmt", ["mxfp4", "fp8"])
+def test_q_producer_bit_exact(ci, neox, fmt):
+    pos, q, cos_sin, w, QP = _producer_inputs(3000, seed=17)
+    code = ci.Q_MXFP4 if fmt == "mxfp4" else ci.Q_FP8
+    got = _run_producer(ci, pos, q, cos_sin, w, neox, code)
+    want = QP.produce(pos.numpy(), q.view(torch.uint16).numpy(), cos_sin.numpy(), w.numpy(), 0.0625, 0.125, neox, fmt)
+    np.testing.assert_array_equal(got[0], want[0])
+    if fmt == "mxfp4":
+        np.testing.assert_array_equal(got[1], want[1])
+    np.testing.assert_array_equal(got[2].view(np.uint32), want[2].view(np.uint32))
+
+
+@needs_cuda
+def test_q_producer_bad_position_flags_without_fault(ci):
+    pos, q, cos_sin, w, QP = _producer_inputs(40, seed=3, max_pos=100)
+    pos[7] = 100
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_out, q_sf, _ = _run_producer(ci, pos, q, cos_sin, w, True, ci.Q_MXFP4, dev_err=err)
+    assert int(err.item()) & ci.DEVERR_POS
+    assert not q_out[7].any()
+
+
+@needs_cuda
+def test_q_producer_feeds_the_indexer(ci):
+    """bf16 queries -> producer -> indexer step, against the producer oracle
+    followed by the indexer oracle: the path from the step before it."""
+    lens = [3000 + i for i in range(7)]
+    base = synth.make_workload("prod", synth.LAYOUT_PREFILL, lens, topk_blocks=64, seed=77)
+    layers = []
+    for j, l in enumerate(base.layers):
+        pos, q, cos_sin, w, QP = _producer_inputs(len(lens), seed=900 + j)
+        q_fp4, q_sf, w_out = _run_producer(ci, pos, q, cos_sin, w, True, ci.Q_MXFP4)
+        want = QP.produce(pos.numpy(), q.view(torch.uint16).numpy(), cos_sin.numpy(), w.numpy(), 0.0625, 0.125, True,
+                          "mxfp4")
+        np.testing.assert_array_equal(q_fp4, want[0])
+        layers.append(synth.Layer(torch.from_numpy(q_fp4), torch.from_numpy(q_sf), torch.from_numpy(w_out), l.k_pool))
+    wl = synth.Workload("prod", base.layout, base.seq_len, base.page_table, layers, base.topk_blocks, base.topk)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))

@@ -28,7 +28,8 @@ LAYOUT_PREFILL = 1
 LAYOUT_VARLEN = 2
 KV_FP8, KV_MXFP4 = 0, 1
 PAGE_BYTES = {KV_FP8: 64 * 128 + 64 * 4, KV_MXFP4: 64 * 64 + 64 * 4}
-DEVERR_LEN, DEVERR_PAGE, DEVERR_BLOCK, DEVERR_TIMEOUT, DEVERR_REQ = 1, 2, 4, 8, 16
+DEVERR_LEN, DEVERR_PAGE, DEVERR_BLOCK, DEVERR_TIMEOUT, DEVERR_REQ, DEVERR_POS = 1, 2, 4, 8, 16, 32
+Q_MXFP4, Q_FP8 = 0, 1
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -42,6 +43,7 @@ SIGNATURES = {
     "ci_prefill_tail": [_P, _I32, _P, _I32, _P, _I64, _P, _I32, _P, _P, _I64, _P, _P, _I32, _P, _P],
     "ci_select_sparse": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32,
                          _P, _P, _I64, _P, _P],
+    "ci_q_rope_quant": [_P, _P, _P, _I32, _P, ctypes.c_float, ctypes.c_float, _I32, _I32, _I32, _P, _P, _P, _P, _P],
     "ci_strerror": [ctypes.c_int],
     "ci_version": [],
 }
@@ -187,3 +189,21 @@ def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_le
         int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
         rows, int(max_len), _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(topk), _ptr(out_pos),
         _ptr(out_score), int(out_pos.stride(0)), _ptr(dev_err), _stream(stream)))
+
+
+def ci_q_rope_quant(positions, q, cos_sin, w, softmax_scale, head_scale, is_neox, out_format, q_out, q_sf, w_out,
+                    dev_err=None, stream=None):
+    """The query producer: RoPE, quantization, head-weight scaling (see include/ci.h)."""
+    _expect(positions, torch.int32, "positions")
+    _expect(q, torch.bfloat16, "q")
+    _expect(cos_sin, torch.float32, "cos_sin")
+    _expect(w, torch.float32, "w")
+    _expect(q_out, torch.uint8, "q_out")
+    _expect(w_out, torch.float32, "w_out")
+    if q_sf is not None:
+        _expect(q_sf, torch.uint8, "q_sf")
+    tokens = int(positions.shape[0])
+    _check("ci_q_rope_quant", lib.ci_q_rope_quant(
+        _ptr(positions), _ptr(q), _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(w), float(softmax_scale),
+        float(head_scale), int(bool(is_neox)), tokens, int(out_format), _ptr(q_out), _ptr(q_sf), _ptr(w_out),
+        _ptr(dev_err), _stream(stream)))

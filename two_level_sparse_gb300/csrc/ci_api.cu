@@ -86,7 +86,7 @@ int launched(cudaError_t e) { return e == cudaSuccess ? CI_OK : CI_ERR_CUDA; }
 
 extern "C" {
 
-int ci_version(void) { return 200; }
+int ci_version(void) { return 201; }
 
 const char* ci_strerror(int status) {
   switch (status) {
@@ -163,6 +163,20 @@ int ci_prefill_tail(const int32_t* req_row_start, int32_t num_req, const int32_t
   ci::TailArgs a{req_row_start, num_req, tail_len,   rows,    blocks,    blocks_stride, nvalid, topk_blocks,
                  out_row,       out_blocks, out_blocks_stride, out_nvalid, out_count, out_cap, dev_err};
   return launched(ci::launch_tail(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ci_q_rope_quant(const int32_t* positions, const uint16_t* q, const float* cos_sin, int32_t max_pos,
+                    const float* w, float softmax_scale, float head_scale, int32_t is_neox, int32_t tokens,
+                    int32_t out_format, uint8_t* q_out, uint8_t* q_sf, float* w_out, int32_t* dev_err, void* stream) {
+  if (tokens < 0 || max_pos < 0) return CI_ERR_SHAPE;
+  if (out_format != CI_Q_MXFP4 && out_format != CI_Q_FP8) return CI_ERR_UNSUPPORTED;
+  if (tokens == 0) return CI_OK;
+  if (!positions || !q || !cos_sin || !w || !q_out || !w_out) return CI_ERR_NULL;
+  if (out_format == CI_Q_MXFP4 && !q_sf) return CI_ERR_NULL;
+  if (q_sf != nullptr && !aligned(q_sf, 4)) return CI_ERR_ALIGN;
+  ci::QProdArgs a{positions, q,      cos_sin, max_pos, w,    softmax_scale, head_scale, tokens,
+                  is_neox != 0, out_format == CI_Q_FP8, q_out, q_sf, w_out, dev_err};
+  return launched(ci::launch_qprod(a, static_cast<cudaStream_t>(stream)));
 }
 
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,

@@ -31,7 +31,8 @@ template <int KV>
 __host__ __device__ constexpr int page_bytes() {
   return page_value_bytes<KV>() + kPage * 4;
 }
-constexpr uint32_t kDevErrLen = 1u, kDevErrPage = 2u, kDevErrBlock = 4u, kDevErrTimeout = 8u, kDevErrReq = 16u;
+constexpr uint32_t kDevErrLen = 1u, kDevErrPage = 2u, kDevErrBlock = 4u, kDevErrTimeout = 8u, kDevErrReq = 16u,
+                   kDevErrPos = 32u;
 constexpr int kLayoutDecode = 0, kLayoutPrefill = 1, kLayoutVarlen = 2;
 
 __device__ __forceinline__ void report(int32_t* dev_err, uint32_t bits) {

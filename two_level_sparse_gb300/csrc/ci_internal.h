@@ -82,7 +82,23 @@ struct TailArgs {
   int32_t* dev_err;
 };
 
+struct QProdArgs {
+  const int32_t* positions;
+  const uint16_t* q;  // bf16 [tokens][64][128]
+  const float* cos_sin;  // [max_pos][64]: 32 cos, then 32 sin
+  int32_t max_pos;
+  const float* w;
+  float softmax_scale, head_scale;
+  int32_t tokens;
+  bool neox, fp8;
+  uint8_t* q_out;
+  uint8_t* q_sf;
+  float* w_out;
+  int32_t* dev_err;
+};
+
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
+cudaError_t launch_qprod(const QProdArgs& a, cudaStream_t stream);
 cudaError_t launch_tail(const TailArgs& a, cudaStream_t stream);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 
