@@ -261,7 +261,8 @@ CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const flo
  *               the weight as the pages print it.
  * A position outside [0, max_pos) sets CI_DEVERR_POS and the token's heads are
  * produced from zeros.  positions int32 [tokens]; cos_sin float [max_pos][64];
- * w, w_out float [tokens][64]; all device memory; q_sf 4-byte aligned.
+ * w, w_out float [tokens][64]; all device memory; q 8-byte, cos_sin 16-byte,
+ * q_out and q_sf 4-byte aligned.
  */
 CI_API int ci_q_rope_quant(const int32_t* positions, const uint16_t* q, const float* cos_sin, int32_t max_pos,
                            const float* w, float softmax_scale, float head_scale, int32_t is_neox, int32_t tokens,

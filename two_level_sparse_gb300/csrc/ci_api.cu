@@ -173,7 +173,8 @@ int ci_q_rope_quant(const int32_t* positions, const uint16_t* q, const float* co
   if (tokens == 0) return CI_OK;
   if (!positions || !q || !cos_sin || !w || !q_out || !w_out) return CI_ERR_NULL;
   if (out_format == CI_Q_MXFP4 && !q_sf) return CI_ERR_NULL;
-  if (q_sf != nullptr && !aligned(q_sf, 4)) return CI_ERR_ALIGN;
+  if ((q_sf != nullptr && !aligned(q_sf, 4)) || !aligned(q, 8) || !aligned(cos_sin, 16) || !aligned(q_out, 4))
+    return CI_ERR_ALIGN;
   ci::QProdArgs a{positions, q,      cos_sin, max_pos, w,    softmax_scale, head_scale, tokens,
                   is_neox != 0, out_format == CI_Q_FP8, q_out, q_sf, w_out, dev_err};
   return launched(ci::launch_qprod(a, static_cast<cudaStream_t>(stream)));

@@ -16,9 +16,8 @@
 //   into the weight: w_out = w * scale * softmax_scale * head_scale.
 // ceil(log2(v)) is taken exactly from the bits of v.
 //
-// One warp per (token, head): lane l holds the rotated pair i = l and dims
-// 64 + l, 96 + l.  Memory-bound: 256 bytes in, 68 (MXFP4) or 128 (FP8) out
-// per head.
+// One warp per eight heads of a token, lane l holding dims 4l .. 4l + 3 of each.
+// Memory-bound: 256 bytes in, 68 (MXFP4) or 128 (FP8) out per head.
 #include <cuda_bf16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -30,18 +29,10 @@ namespace ci {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kHeadsPerWarp = 8;  // loads of eight heads in flight per warp before any is processed
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-__device__ __forceinline__ float warp_absmax(float v) {
-  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
-}
-__device__ __forceinline__ float half_absmax(float v) {  // over the 16 lanes of this half-warp
-  float m = fabsf(v);
-#pragma unroll
-  for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  return m;
-}
 // Exact ceil(log2(max(amax, 1e-10) * (1 / vmax))).
 __device__ __forceinline__ int scale_exp(float amax, float inv_vmax) {
   const uint32_t u = __float_as_uint(__fmul_rn(fmaxf(amax, 1e-10f), inv_vmax));
@@ -60,79 +51,114 @@ __device__ __forceinline__ uint8_t e4m3(float x) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
 }
 
+// Lane l loads dims 4l .. 4l + 3 of the head (one 8-byte load per lane, the
+// head's 256 bytes per warp instruction).  Lanes 0-15 hold the rotated half:
+// in the NeoX layout lane l < 8 holds x0 of pairs 4l .. 4l + 3 and lane l + 8
+// their x1 (exchanged by one shuffle); in the interleaved layout lane l holds
+// both elements of pairs 2l and 2l + 1.  Lanes 16-31 hold dims 64..127.  The
+// 32-dim blocks are the lane octets 0-7, 8-15, 16-23, 24-31.
 template <bool kFp8, bool kNeox>
-__global__ void __launch_bounds__(32 * kWarpsPerBlock) qprod_kernel(const QProdArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (gw >= static_cast<int64_t>(a.tokens) * kHeads) return;
-  const int t = static_cast<int>(gw / kHeads);
-  const int pos = a.positions[t];
-  const bool ok = pos >= 0 && pos < a.max_pos;
-  if (!ok && lane == 0 && (gw % kHeads) == 0) report(a.dev_err, kDevErrPos);
-  const uint16_t* q = a.q + gw * kDim;
-  auto ld = [&](int d) { return ok ? __uint_as_float(static_cast<uint32_t>(q[d]) << 16) : 0.0f; };
-  const float c = ok ? a.cos_sin[static_cast<int64_t>(pos) * 64 + lane] : 0.0f;
-  const float s = ok ? a.cos_sin[static_cast<int64_t>(pos) * 64 + 32 + lane] : 0.0f;
-  const float x0 = kNeox ? ld(lane) : ld(2 * lane), x1 = kNeox ? ld(32 + lane) : ld(2 * lane + 1);
-  const float r0 = bf16_round(__fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s)));
-  const float r1 = bf16_round(__fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s)));
-  const float n0 = ld(64 + lane), n1 = ld(96 + lane);
+__device__ __forceinline__ void qprod_head(const QProdArgs& a, int64_t gw, int lane, uint2 raw, const float (&cc)[4],
+                                           const float (&ss)[4]) {
+  float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u), __uint_as_float(raw.y << 16),
+                __uint_as_float(raw.y & 0xFFFF0000u)};
+  float v[4];  // this lane's four output dims, in order
+  {
+    // the partner values of the other half of each NeoX pair
+    float pr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pr[j] = __shfl_xor_sync(0xffffffffu, x[j], 8);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = x[j];
+    if (lane < 16) {
+      if (kNeox) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float x0 = lane < 8 ? x[j] : pr[j], x1 = lane < 8 ? pr[j] : x[j];
+          v[j] = lane < 8 ? bf16_round(__fsub_rn(__fmul_rn(x0, cc[j]), __fmul_rn(x1, ss[j])))
+                          : bf16_round(__fadd_rn(__fmul_rn(x1, cc[j]), __fmul_rn(x0, ss[j])));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float x0 = x[2 * j], x1 = x[2 * j + 1];
+          v[2 * j] = bf16_round(__fsub_rn(__fmul_rn(x0, cc[j]), __fmul_rn(x1, ss[j])));
+          v[2 * j + 1] = bf16_round(__fadd_rn(__fmul_rn(x1, cc[j]), __fmul_rn(x0, ss[j])));
+        }
+      }
+    }
+  }
+  const float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
   const float w = a.w[gw];
   if (kFp8) {
-    const float amax = warp_absmax(fmaxf(fmaxf(fabsf(r0), fabsf(r1)), fmaxf(fabsf(n0), fabsf(n1))));
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
     const int e = scale_exp(amax, 1.0f / 448.0f);
-    auto q8 = [&](float x) { return e4m3(fminf(fmaxf(unscale(x, e), -448.0f), 448.0f)); };
-    uint8_t* o = a.q_out + gw * kDim;
-    o[kNeox ? lane : 2 * lane] = q8(r0);
-    o[kNeox ? 32 + lane : 2 * lane + 1] = q8(r1);
-    o[64 + lane] = q8(n0);
-    o[96 + lane] = q8(n1);
-    if (lane == 0)
-      a.w_out[gw] = __fmul_rn(__fmul_rn(__fmul_rn(w, pow2i(e)), a.softmax_scale), a.head_scale);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      packed |= static_cast<uint32_t>(e4m3(fminf(fmaxf(unscale(v[j], e), -448.0f), 448.0f))) << (8 * j);
+    *reinterpret_cast<uint32_t*>(a.q_out + gw * kDim + 4 * lane) = packed;
+    if (lane == 0) a.w_out[gw] = __fmul_rn(__fmul_rn(__fmul_rn(w, pow2i(e)), a.softmax_scale), a.head_scale);
   } else {
-    // blocks of 32 dims: NeoX r0 | r1 | n0 | n1 across the lanes; interleaved
-    // (r0, r1) of lanes 0-15 | of lanes 16-31 | n0 | n1
-    float m01a, m01b;
-    if (kNeox) {
-      m01a = warp_absmax(r0);
-      m01b = warp_absmax(r1);
-    } else {
-      const float m = half_absmax(fmaxf(fabsf(r0), fabsf(r1)));
-      m01a = __shfl_sync(0xffffffffu, m, 0);
-      m01b = __shfl_sync(0xffffffffu, m, 16);
-    }
-    const int e0 = scale_exp(m01a, 1.0f / 6.0f), e1 = scale_exp(m01b, 1.0f / 6.0f);
-    const int e2 = scale_exp(warp_absmax(n0), 1.0f / 6.0f), e3 = scale_exp(warp_absmax(n1), 1.0f / 6.0f);
-    uint8_t* o = a.q_out + gw * (kDim / 2);
-    // a byte holds dims (2m, 2m + 1): the pair of neighbouring lanes, written by the even lane
-    auto put_pair = [&](float v, int e, int byte0) {
-      const float y = unscale(v, e);
-      const float yn = __shfl_xor_sync(0xffffffffu, y, 1);
-      if ((lane & 1) == 0) o[byte0 + (lane >> 1)] = e2m1_pair(y, yn);
-    };
-    if (kNeox) {
-      put_pair(r0, e0, 0);
-      put_pair(r1, e1, 16);
-    } else {
-      const int e = lane < 16 ? e0 : e1;
-      o[lane] = e2m1_pair(unscale(r0, e), unscale(r1, e));
-    }
-    put_pair(n0, e2, 32);
-    put_pair(n1, e3, 48);
+    float bm = m;  // block maximum over this lane's octet
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+    const int e = scale_exp(bm, 1.0f / 6.0f);
+    const uint32_t lo = e2m1_pair(unscale(v[0], e), unscale(v[1], e));
+    const uint32_t hi = e2m1_pair(unscale(v[2], e), unscale(v[3], e));
+    *reinterpret_cast<uint16_t*>(a.q_out + gw * (kDim / 2) + 2 * lane) = static_cast<uint16_t>(lo | (hi << 8));
+    const int e1 = __shfl_sync(0xffffffffu, e, 8), e2 = __shfl_sync(0xffffffffu, e, 16),
+              e3 = __shfl_sync(0xffffffffu, e, 24);
     if (lane == 0) {
       *reinterpret_cast<uint32_t*>(a.q_sf + gw * 4) =
-          static_cast<uint32_t>(e0 + 127) | (static_cast<uint32_t>(e1 + 127) << 8) |
+          static_cast<uint32_t>(e + 127) | (static_cast<uint32_t>(e1 + 127) << 8) |
           (static_cast<uint32_t>(e2 + 127) << 16) | (static_cast<uint32_t>(e3 + 127) << 24);
       a.w_out[gw] = __fmul_rn(__fmul_rn(w, a.softmax_scale), a.head_scale);
     }
   }
 }
 
+// Each warp takes kHeadsPerWarp consecutive heads of one token (64 is a
+// multiple), their loads issued before any is processed.
+template <bool kFp8, bool kNeox>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock) qprod_kernel(const QProdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t g0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * kHeadsPerWarp;
+  if (g0 >= static_cast<int64_t>(a.tokens) * kHeads) return;
+  const int t = static_cast<int>(g0 / kHeads);
+  const int pos = a.positions[t];
+  const bool ok = pos >= 0 && pos < a.max_pos;
+  if (!ok && lane == 0 && (g0 % kHeads) == 0) report(a.dev_err, kDevErrPos);
+  uint2 raw[kHeadsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kHeadsPerWarp; ++k)
+    raw[k] = ok ? *reinterpret_cast<const uint2*>(a.q + (g0 + k) * kDim + 4 * lane) : make_uint2(0, 0);
+  // cos / sin of this lane's pairs (NeoX lanes 0-15: pairs 4 (l % 8) ..; interleaved
+  // lanes 0-15: pairs 2l, 2l + 1), zeros for a bad position
+  float cc[4] = {0.f, 0.f, 0.f, 0.f}, ss[4] = {0.f, 0.f, 0.f, 0.f};
+  if (ok && lane < 16) {
+    const float* cs = a.cos_sin + static_cast<int64_t>(pos) * 64;
+    if (kNeox) {
+      const int i0 = 4 * (lane & 7);
+      const float4 c = *reinterpret_cast<const float4*>(cs + i0), sn = *reinterpret_cast<const float4*>(cs + 32 + i0);
+      cc[0] = c.x, cc[1] = c.y, cc[2] = c.z, cc[3] = c.w;
+      ss[0] = sn.x, ss[1] = sn.y, ss[2] = sn.z, ss[3] = sn.w;
+    } else {
+      const int i0 = 2 * lane;
+      const float2 c = *reinterpret_cast<const float2*>(cs + i0), sn = *reinterpret_cast<const float2*>(cs + 32 + i0);
+      cc[0] = c.x, cc[1] = c.y;
+      ss[0] = sn.x, ss[1] = sn.y;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kHeadsPerWarp; ++k) qprod_head<kFp8, kNeox>(a, g0 + k, lane, raw[k], cc, ss);
+}
+
 }  // namespace
 
 cudaError_t launch_qprod(const QProdArgs& a, cudaStream_t stream) {
   if (a.tokens == 0) return cudaSuccess;
-  const int64_t warps = static_cast<int64_t>(a.tokens) * kHeads;
+  const int64_t warps = static_cast<int64_t>(a.tokens) * kHeads / kHeadsPerWarp;
   const unsigned grid = static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
   const int threads = 32 * kWarpsPerBlock;
   if (a.fp8) {
