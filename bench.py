@@ -350,6 +350,34 @@ def measure_mxfp4(steps, stream, flush, world, peaks):
     return line
 
 
+def measure_dcp(steps, stream, flush, world):
+    """The headline chunk as ``world`` context shards emulated on this device:
+    every shard's dense pass and selects run here, one after another, with
+    the two merges in between (on ``world`` devices the shards would run side
+    by side and the merges would be collectives).  The outputs equal the
+    unsharded step's; the time shows what the sharded form costs on one
+    device."""
+    from two_level_sparse_gb300 import synth
+    from two_level_sparse_gb300.dcp import DcpStep
+
+    wl = synth.config_workload(HEADLINE_CID, device="cuda")
+    d = DcpStep(wl, world, with_scores=False)
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(steps + 1):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            d.run(stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 1:
+                ms.append(e0.elapsed_time(e1))
+    return {"metric": f"indexer ms per 16K-token prefill chunk @262K ctx, {world} context shards on one GPU",
+            "workload": wl.name + f"_dcp{world}", "value": statistics.mean(ms), "unit": "ms",
+            "dev_err": int(d.dev_err.item())}
+
+
 QPROD_TOKENS = 16384
 
 
@@ -514,6 +542,8 @@ def main():
         secondary.append(measure_mxfp4(max(3, args.steps // 2), stream, flush, world, peaks))
         torch.cuda.empty_cache()
         secondary.append(measure_qprod(max(3, args.steps // 2), stream, flush, peaks))
+        torch.cuda.empty_cache()
+        secondary.append(measure_dcp(3, stream, flush, 2))
         torch.cuda.empty_cache()
 
     cpu_ms, cpu_rows, cpu_threads, nrows = (None, 0, 0, 0)

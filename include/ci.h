@@ -19,6 +19,9 @@
  *                            reading the keys once;
  *     ci_prefill_tail        the published table of the last rows of each
  *                            request of a multi-request chunk;
+ *   context sharding (one device emulating W shards):
+ *     ci_dcp_merge_keys      shards' local block maxima -> global keys;
+ *     ci_dcp_merge_topk      shards' local top-k -> global top-k;
  *   before level one, once per layer:
  *     ci_q_rope_quant        the query producer: RoPE, quantization to the
  *                            indexer's query format, head-weight scaling;
@@ -142,14 +145,22 @@ enum ci_q_format { CI_Q_MXFP4 = 0, CI_Q_FP8 = 1 };
  * topk blocks skipped).  The [rows, L] score matrix is never written.
  *
  * keys: float [rows][keys_stride], 16-byte aligned, keys_stride % 8 == 0 and
- * keys_stride >= ceil(max_len / 8).
+ * keys_stride >= ceil(max_len / block_positions).
+ *
+ * block_positions is 8 for the method's blocks.  A shard of a context-sharded
+ * indexer (vLLM sparse_attn_indexer.py, two-level candidate filtering under
+ * DCP: W shards, interleave 1, position s on shard s % W at local position
+ * s / W) passes its local pool and lengths with block_positions = 8 / W (4, 2
+ * or 1; FP8 pages): key b is then the maximum over local positions
+ * [b * block_positions, (b + 1) * block_positions), its part of global block b,
+ * and no key is pinned to +inf (ci_dcp_merge_keys pins the global newest block).
  */
 CI_API int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                          int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
                          int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
                          int32_t max_len,
-                         int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
-                         void* stream);
+                         int32_t skip_le_blocks, int32_t block_positions, float* keys, int64_t keys_stride,
+                         int32_t* dev_err, void* stream);
 
 /*
  * Level one, publishing: each row's candidate blocks.
@@ -228,15 +239,50 @@ CI_API int ci_prefill_tail(const int32_t* req_row_start, int32_t num_req, const 
  *
  * blocks: int32 [rows][blocks_stride]; nvalid: int32 [rows], each
  * 0 <= nvalid[t] <= max_blocks <= min(blocks_stride, 2176).
- * 1 <= topk <= 2048, topk <= out_stride; num_pages <= 2^24.
+ * 1 <= topk <= 2048, topk <= out_stride; num_pages <= 2^21.
+ *
+ * block_positions is 8 for the method's blocks; a shard of a context-sharded
+ * indexer (see ci_score_dense_amax8) passes 8 / W: block id b then names its
+ * local positions [b * block_positions, (b + 1) * block_positions), and the
+ * output positions are local.
  */
 CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                      int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
                      int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
                      int32_t max_len,
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
-                     int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
-                     void* stream);
+                     int32_t block_positions, int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride,
+                     int32_t* dev_err, void* stream);
+
+/*
+ * The exchange steps of a context-sharded indexer with W = world shards
+ * (2, 4 or 8; interleave 1), run on one device over all shards' buffers
+ * (vLLM sparse_attn_indexer.py: the producer MAX-reduces block scores across
+ * ranks and pins the global newest block; _merge_dcp_topk_global merges each
+ * rank's local top-K exactly).
+ *
+ * ci_dcp_merge_keys: keys_local[r * rank_stride + t * local_stride + b] are
+ * shard r's local block maxima (ci_score_dense_amax8 with block_positions =
+ * 8 / W and skip_le_blocks = 0).  For every row t with nb_t = ceil(L_t / 8) >
+ * skip_le_blocks (seq_len = the global lengths) writes keys[t * keys_stride +
+ * b], b < nb_t: the maximum over the shards that hold a position of global
+ * block b, and +inf for b = nb_t - 1 -- exactly the keys ci_score_dense_amax8
+ * writes for the unsharded row.  keys_stride, local_stride >= ceil(max_len/8).
+ *
+ * ci_dcp_merge_topk: pos_local / score_local[r * rank_stride + t *
+ * local_stride + i], i < topk, are shard r's ci_select_sparse outputs (local
+ * positions ascending, -1 padded, with their scores).  Writes out_pos[t *
+ * out_stride + i], i < topk: the topk best of all shards' candidates (global
+ * position = local * W + r; ties toward the lower position), ascending, -1
+ * padded, and their scores to out_score if it is not NULL.  world * topk <=
+ * 4096.
+ */
+CI_API int ci_dcp_merge_keys(const float* keys_local, int32_t world, int64_t rank_stride, int64_t local_stride,
+                             const int32_t* seq_len, int32_t rows, int32_t max_len, int32_t skip_le_blocks,
+                             float* keys, int64_t keys_stride, int32_t* dev_err, void* stream);
+CI_API int ci_dcp_merge_topk(const int32_t* pos_local, const float* score_local, int32_t world, int64_t rank_stride,
+                             int64_t local_stride, int32_t rows, int32_t topk, int32_t* out_pos, float* out_score,
+                             int64_t out_stride, void* stream);
 
 /*
  * The query producer (vLLM indexer.py page, rope_quant_q; the

@@ -29,8 +29,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(
-        ["ci_prefill_tail", "ci_publish_blocks", "ci_publish_blocks2", "ci_q_rope_quant", "ci_score_dense_amax8",
-         "ci_select_sparse", "ci_strerror", "ci_version"])
+        ["ci_dcp_merge_keys", "ci_dcp_merge_topk", "ci_prefill_tail", "ci_publish_blocks", "ci_publish_blocks2",
+         "ci_q_rope_quant", "ci_score_dense_amax8", "ci_select_sparse", "ci_strerror", "ci_version"])
 
 
 def test_library_exports_every_declared_symbol(ci):
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(ci):
 
 
 def test_status_names(ci):
-    assert ci.version() == 201
+    assert ci.version() == 300
     assert ci.strerror(0) == "ok"
     for code in ci.CI_ERR:
         assert ci.strerror(code) != "unknown status"
@@ -54,30 +54,33 @@ N = None
 def test_dense_host_checks(ci):
     f = ci.lib.ci_score_dense_amax8
     # rows == 0: nothing to do, even with null pointers
-    assert f(N, N, N, N, 1, 0, N, 0, 1, 0, N, N, 0, 0, 0, N, 8, N, N) == 0
+    assert f(N, N, N, N, 1, 0, N, 0, 1, 0, N, N, 0, 0, 0, 8, N, 8, N, N) == 0
     # null pointer
-    assert f(N, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -1
+    assert f(N, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, 8, P, 8, N, N) == -1
     # bad layout
-    assert f(P, P, P, P, 1, 0, P, 2, 1, 7, N, P, 2, 64, 0, P, 8, N, N) == -5
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 7, N, P, 2, 64, 0, 8, P, 8, N, N) == -5
     # decode needs one request per row
-    assert f(P, P, P, P, 1, 0, P, 3, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 3, 1, 0, N, P, 2, 64, 0, 8, P, 8, N, N) == -2
     # prefill needs exactly one request
-    assert f(P, P, P, P, 1, 0, P, 2, 1, 1, N, P, 2, 64, 0, P, 8, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 1, N, P, 2, 64, 0, 8, P, 8, N, N) == -2
     # several requests: row starts required, 1..4096 requests
-    assert f(P, P, P, P, 1, 0, P, 2, 1, 2, N, P, 2, 64, 0, P, 8, N, N) == -1
-    assert f(P, P, P, P, 1, 0, P, 0, 1, 2, P, P, 2, 64, 0, P, 8, N, N) == -4
-    assert f(P, P, P, P, 1, 0, P, 5000, 1, 2, P, P, 2, 64, 0, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 2, N, P, 2, 64, 0, 8, P, 8, N, N) == -1
+    assert f(P, P, P, P, 1, 0, P, 0, 1, 2, P, P, 2, 64, 0, 8, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 0, P, 5000, 1, 2, P, P, 2, 64, 0, 8, P, 8, N, N) == -4
     # max_len beyond the page table
-    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 65, 0, P, 16, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 65, 0, 8, P, 16, N, N) == -2
     # keys stride not a multiple of 8 / too short
-    assert f(P, P, P, P, 1, 0, P, 2, 2, 0, N, P, 2, 128, 0, P, 12, N, N) == -2
-    assert f(P, P, P, P, 1, 0, P, 2, 4, 0, N, P, 2, 256, 0, P, 8, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 2, 0, N, P, 2, 128, 0, 8, P, 12, N, N) == -2
+    assert f(P, P, P, P, 1, 0, P, 2, 4, 0, N, P, 2, 256, 0, 8, P, 8, N, N) == -2
     # misaligned pool
-    assert f(P, P, P, ctypes.c_void_p(0x1001), 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -3
+    assert f(P, P, P, ctypes.c_void_p(0x1001), 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, 8, P, 8, N, N) == -3
     # unknown K page format
-    assert f(P, P, P, P, 1, 2, P, 2, 1, 0, N, P, 2, 64, 0, P, 8, N, N) == -5
+    assert f(P, P, P, P, 1, 2, P, 2, 1, 0, N, P, 2, 64, 0, 8, P, 8, N, N) == -5
+    # block size other than 8, 4, 2, 1; local blocks need FP8 pages
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, 0, 3, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 1, P, 2, 1, 0, N, P, 2, 64, 0, 4, P, 8, N, N) == -5
     # negative skip
-    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, -1, P, 8, N, N) == -4
+    assert f(P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, -1, 8, P, 8, N, N) == -4
 
 
 def test_publish_host_checks(ci):
@@ -154,19 +157,19 @@ def test_q_rope_quant_host_checks(ci):
 
 def test_select_host_checks(ci):
     f = ci.lib.ci_select_sparse
-    ok_args = [P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, P, 16, P, 16, 8, P, N, 8, N, N]
+    ok_args = [P, P, P, P, 1, 0, P, 2, 1, 0, N, P, 2, 64, P, 16, P, 16, 8, 8, P, N, 8, N, N]
     assert f(*ok_args[:12], 0, *ok_args[13:]) == 0  # rows == 0
     bad = list(ok_args)
-    bad[18] = 0  # topk < 1
+    bad[19] = 0  # topk < 1
     assert f(*bad) == -4
     bad = list(ok_args)
     bad[17] = 5000  # max_blocks too large
     assert f(*bad) == -4
     bad = list(ok_args)
-    bad[21] = 4  # out stride < topk
+    bad[22] = 4  # out stride < topk
     assert f(*bad) == -2
     bad = list(ok_args)
-    bad[19] = N  # no output
+    bad[20] = N  # no output
     assert f(*bad) == -1
     bad = list(ok_args)
     bad[9] = 2  # several requests without row starts
@@ -174,3 +177,16 @@ def test_select_host_checks(ci):
     bad = list(ok_args)
     bad[5] = 3  # unknown K page format
     assert f(*bad) == -5
+    bad = list(ok_args)
+    bad[18] = 16  # block size other than 8, 4, 2, 1
+    assert f(*bad) == -4
+
+
+def test_dcp_merge_host_checks(ci):
+    fk, ft = ci.lib.ci_dcp_merge_keys, ci.lib.ci_dcp_merge_topk
+    assert fk(P, 3, 64, 8, P, 4, 64, 0, P, 8, N, N) == -4   # world not 2, 4 or 8
+    assert fk(P, 2, 16, 8, P, 4, 64, 0, P, 8, N, N) == -2   # shards overlap
+    assert fk(P, 2, 0, 8, P, 0, 64, 0, P, 8, N, N) == 0     # no rows
+    assert fk(N, 2, 64, 8, P, 4, 64, 0, P, 8, N, N) == -1
+    assert ft(P, P, 8, 4096, 1024, 4, 1024, P, N, 1024, N) == -4  # 8 x 1024 candidates
+    assert ft(P, P, 2, 4096, 512, 8, 600, P, N, 600, N) == -2   # local stride < topk

@@ -546,3 +546,36 @@ def test_q_producer_feeds_the_indexer(ci):
     step = run_step(wl)
     assert int(step.dev_err.item()) == 0
     assert_ok(compare.check_step(wl, step.outputs_numpy()))
+
+
+# ----------------------------------------------------------------------------- context sharding (one device)
+@needs_cuda
+@pytest.mark.parametrize("world", [2, 4, 8])
+@pytest.mark.parametrize("case", ["decode", "prefill", "varlen"])
+def test_dcp_step_equals_unsharded_step_bitwise(ci, world, case):
+    """W context shards (interleave 1): local block maxima merged across shards,
+    local top-512 merged across shards -- the same keys, blocks, positions and
+    scores as the unsharded step, bit for bit."""
+    from two_level_sparse_gb300.dcp import DcpStep
+    from two_level_sparse_gb300.step import IndexerStep
+
+    if case == "decode":
+        wl = synth.make_workload("dcp", synth.LAYOUT_DECODE, [0, 1, 7, 8, 9, 100, 2100, 20000], 128, seed=31)
+    elif case == "prefill":
+        wl = synth.make_workload("dcp", synth.LAYOUT_PREFILL, [3000 + i for i in range(7)], 64, seed=32)
+    else:
+        wl = synth.make_varlen_workload("dcp", (300, 2040, 0, 5000), (4, 1, 2, 5), 64, seed=33)
+    dev = wl.to("cuda")
+    ref = IndexerStep(dev, with_scores=True)
+    ref.run()
+    d = DcpStep(dev, world)
+    d.run()
+    torch.cuda.synchronize()
+    assert int(d.dev_err.item()) == 0 and int(ref.dev_err.item()) == 0
+    a, b = ref.outputs_numpy(), d.outputs_numpy()
+    for k in ("blocks", "nvalid", "blocks_src", "nvalid_src", "pos"):
+        np.testing.assert_array_equal(b[k], a[k], err_msg=k)
+    np.testing.assert_array_equal(b["score"].view(np.uint32), a["score"].view(np.uint32))
+    nb = (wl.seq_len.numpy() + 7) // 8
+    for t in np.nonzero(nb > min(wl.topk_blocks, wl.topk + 1))[0]:
+        np.testing.assert_array_equal(b["keys"][t, : nb[t]].view(np.uint32), a["keys"][t, : nb[t]].view(np.uint32))

@@ -36,13 +36,15 @@ _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 
 SIGNATURES = {
-    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _I64, _P,
-                             _P],
+    "ci_score_dense_amax8": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _I64,
+                             _P, _P],
     "ci_publish_blocks": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P, _P],
     "ci_publish_blocks2": [_P, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _P],
     "ci_prefill_tail": [_P, _I32, _P, _I32, _P, _I64, _P, _I32, _P, _P, _I64, _P, _P, _I32, _P, _P],
     "ci_select_sparse": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32,
-                         _P, _P, _I64, _P, _P],
+                         _I32, _P, _P, _I64, _P, _P],
+    "ci_dcp_merge_keys": [_P, _I32, _I64, _I64, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
+    "ci_dcp_merge_topk": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _I64, _P],
     "ci_q_rope_quant": [_P, _P, _P, _I32, _P, ctypes.c_float, ctypes.c_float, _I32, _I32, _I32, _P, _P, _P, _P, _P],
     "ci_strerror": [ctypes.c_int],
     "ci_version": [],
@@ -117,7 +119,7 @@ def _req_start(layout, req_start):
 
 
 def ci_score_dense_amax8(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, skip_le_blocks, keys,
-                         dev_err=None, stream=None, req_start=None):
+                         dev_err=None, stream=None, req_start=None, block_positions=8):
     """Block keys of the source layer (see include/ci.h)."""
     for t, d, n in ((q_fp4, torch.uint8, "q_fp4"), (q_sf, torch.uint8, "q_sf"), (w, torch.float32, "w"),
                     (k_pool, torch.uint8, "k_pool"), (page_table, torch.int32, "page_table"),
@@ -127,7 +129,8 @@ def ci_score_dense_amax8(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, ma
     _check("ci_score_dense_amax8", lib.ci_score_dense_amax8(
         _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), kv_format(k_pool), _ptr(page_table),
         int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
-        rows, int(max_len), int(skip_le_blocks), _ptr(keys), int(keys.stride(0)) if keys.dim() == 2 else 0,
+        rows, int(max_len), int(skip_le_blocks), int(block_positions), _ptr(keys),
+        int(keys.stride(0)) if keys.dim() == 2 else 0,
         _ptr(dev_err), _stream(stream)))
 
 
@@ -174,7 +177,7 @@ def ci_prefill_tail(req_start, tail_len, blocks, nvalid, out_row, out_blocks, ou
 
 
 def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_len, blocks, nvalid, max_blocks, topk,
-                     out_pos, out_score=None, dev_err=None, stream=None, req_start=None):
+                     out_pos, out_score=None, dev_err=None, stream=None, req_start=None, block_positions=8):
     """A layer's top-k positions inside the candidate blocks (see include/ci.h)."""
     for t, d, n in ((q_fp4, torch.uint8, "q_fp4"), (q_sf, torch.uint8, "q_sf"), (w, torch.float32, "w"),
                     (k_pool, torch.uint8, "k_pool"), (page_table, torch.int32, "page_table"),
@@ -187,7 +190,8 @@ def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_le
     _check("ci_select_sparse", lib.ci_select_sparse(
         _ptr(q_fp4), _ptr(q_sf), _ptr(w), _ptr(k_pool), int(k_pool.shape[0]), kv_format(k_pool), _ptr(page_table),
         int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
-        rows, int(max_len), _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(topk), _ptr(out_pos),
+        rows, int(max_len), _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(block_positions),
+        int(topk), _ptr(out_pos),
         _ptr(out_score), int(out_pos.stride(0)), _ptr(dev_err), _stream(stream)))
 
 
@@ -207,3 +211,25 @@ def ci_q_rope_quant(positions, q, cos_sin, w, softmax_scale, head_scale, is_neox
         _ptr(positions), _ptr(q), _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(w), float(softmax_scale),
         float(head_scale), int(bool(is_neox)), tokens, int(out_format), _ptr(q_out), _ptr(q_sf), _ptr(w_out),
         _ptr(dev_err), _stream(stream)))
+
+
+def ci_dcp_merge_keys(keys_local, seq_len, max_len, skip_le_blocks, keys, dev_err=None, stream=None):
+    """Shards' local block maxima ``keys_local[W, rows, stride]`` -> the global keys (see include/ci.h)."""
+    _expect(keys_local, torch.float32, "keys_local")
+    _expect(seq_len, torch.int32, "seq_len")
+    _expect(keys, torch.float32, "keys")
+    world, rows = int(keys_local.shape[0]), int(keys_local.shape[1])
+    _check("ci_dcp_merge_keys", lib.ci_dcp_merge_keys(
+        _ptr(keys_local), world, int(keys_local.stride(0)), int(keys_local.stride(1)), _ptr(seq_len), rows,
+        int(max_len), int(skip_le_blocks), _ptr(keys), int(keys.stride(0)), _ptr(dev_err), _stream(stream)))
+
+
+def ci_dcp_merge_topk(pos_local, score_local, out_pos, out_score=None, stream=None):
+    """Shards' local top-k ``[W, rows, k]`` -> the global top-k (see include/ci.h)."""
+    _expect(pos_local, torch.int32, "pos_local")
+    _expect(score_local, torch.float32, "score_local")
+    _expect(out_pos, torch.int32, "out_pos")
+    world, rows, k = (int(x) for x in pos_local.shape)
+    _check("ci_dcp_merge_topk", lib.ci_dcp_merge_topk(
+        _ptr(pos_local), _ptr(score_local), world, int(pos_local.stride(0)), int(pos_local.stride(1)), rows, k,
+        _ptr(out_pos), _ptr(out_score), int(out_pos.stride(0)), _stream(stream)))

@@ -82,11 +82,22 @@ int check_pool(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const 
 
 int launched(cudaError_t e) { return e == cudaSuccess ? CI_OK : CI_ERR_CUDA; }
 
+// log2 of 8, 4, 2 or 1 positions per block; -1 otherwise.
+int block_shift_of(int32_t block_positions) {
+  switch (block_positions) {
+    case 8: return 3;
+    case 4: return 2;
+    case 2: return 1;
+    case 1: return 0;
+    default: return -1;
+  }
+}
+
 }  // namespace
 
 extern "C" {
 
-int ci_version(void) { return 201; }
+int ci_version(void) { return 300; }
 
 const char* ci_strerror(int status) {
   switch (status) {
@@ -104,18 +115,23 @@ const char* ci_strerror(int status) {
 int ci_score_dense_amax8(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                          int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
                          int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
-                         int32_t max_len, int32_t skip_le_blocks, float* keys, int64_t keys_stride, int32_t* dev_err,
-                         void* stream) {
+                         int32_t max_len, int32_t skip_le_blocks, int32_t block_positions, float* keys,
+                         int64_t keys_stride, int32_t* dev_err, void* stream) {
   int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, num_req, max_pages, layout,
                       req_row_start, seq_len, rows, max_len);
   if (st != CI_OK) return st;
   if (skip_le_blocks < 0) return CI_ERR_RANGE;
+  const int shift = block_shift_of(block_positions);
+  if (shift < 0) return CI_ERR_RANGE;
+  if (shift != 3 && kv_format != CI_KV_FP8) return CI_ERR_UNSUPPORTED;
   if (rows == 0) return CI_OK;
   if (!keys) return CI_ERR_NULL;
-  if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
+  if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + block_positions - 1) >> shift)
+    return CI_ERR_SHAPE;
   if (!aligned(keys, 16)) return CI_ERR_ALIGN;
   ci::DenseArgs a{{q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, max_pages, layout, req_row_start, num_req, seq_len,
                    rows, max_len, dev_err},
+                  shift,
                   skip_le_blocks,
                   keys,
                   keys_stride};
@@ -180,23 +196,54 @@ int ci_q_rope_quant(const int32_t* positions, const uint16_t* q, const float* co
   return launched(ci::launch_qprod(a, static_cast<cudaStream_t>(stream)));
 }
 
+int ci_dcp_merge_keys(const float* keys_local, int32_t world, int64_t rank_stride, int64_t local_stride,
+                      const int32_t* seq_len, int32_t rows, int32_t max_len, int32_t skip_le_blocks, float* keys,
+                      int64_t keys_stride, int32_t* dev_err, void* stream) {
+  if (rows < 0 || max_len < 0) return CI_ERR_SHAPE;
+  if (world != 2 && world != 4 && world != 8) return CI_ERR_RANGE;
+  if (skip_le_blocks < 0) return CI_ERR_RANGE;
+  if (rows == 0) return CI_OK;
+  if (!keys_local || !seq_len || !keys) return CI_ERR_NULL;
+  const int64_t nb = (static_cast<int64_t>(max_len) + 7) / 8;
+  if (keys_stride < nb || local_stride < nb || rank_stride < local_stride * rows) return CI_ERR_SHAPE;
+  ci::DcpKeysArgs a{keys_local, world, rank_stride, local_stride, seq_len, rows, max_len, skip_le_blocks,
+                    keys,       keys_stride, dev_err};
+  return launched(ci::launch_dcp_merge_keys(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ci_dcp_merge_topk(const int32_t* pos_local, const float* score_local, int32_t world, int64_t rank_stride,
+                      int64_t local_stride, int32_t rows, int32_t topk, int32_t* out_pos, float* out_score,
+                      int64_t out_stride, void* stream) {
+  if (rows < 0) return CI_ERR_SHAPE;
+  if (world != 2 && world != 4 && world != 8) return CI_ERR_RANGE;
+  if (topk < 1 || static_cast<int64_t>(topk) * world > 4096) return CI_ERR_RANGE;
+  if (rows == 0) return CI_OK;
+  if (!pos_local || !score_local || !out_pos) return CI_ERR_NULL;
+  if (local_stride < topk || out_stride < topk || rank_stride < local_stride * rows) return CI_ERR_SHAPE;
+  ci::DcpTopkArgs a{pos_local, score_local, world, rank_stride, local_stride, rows, topk, out_pos, out_score, out_stride};
+  return launched(ci::launch_dcp_merge_topk(a, static_cast<cudaStream_t>(stream)));
+}
+
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                      int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
                      const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len,
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
-                     int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride, int32_t* dev_err,
-                     void* stream) {
+                     int32_t block_positions, int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride,
+                     int32_t* dev_err, void* stream) {
   int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, num_req, max_pages, layout,
                       req_row_start, seq_len, rows, max_len);
   if (st != CI_OK) return st;
   if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
   if (max_blocks < 0 || max_blocks > 2176) return CI_ERR_RANGE;
-  if (num_pages > (int64_t{1} << 24)) return CI_ERR_RANGE;  // page ids are packed into 24 bits
+  const int shift = block_shift_of(block_positions);
+  if (shift < 0) return CI_ERR_RANGE;
+  if (num_pages > (int64_t{1} << 21)) return CI_ERR_RANGE;  // page ids are packed into 21 bits
   if (rows == 0) return CI_OK;
   if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
   if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;
   ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, max_pages, layout, req_row_start, num_req, seq_len,
                     rows, max_len, dev_err},
+                   shift,
                    blocks,
                    blocks_stride,
                    nvalid,

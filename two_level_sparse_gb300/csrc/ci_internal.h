@@ -28,6 +28,7 @@ struct PoolArgs {
 
 struct DenseArgs {
   PoolArgs p;
+  int32_t block_shift;  // log2 of the positions per key: 3, or 2/1/0 for a context shard (no +inf pin)
   int32_t skip_le_blocks;
   float* keys;
   int64_t keys_stride;
@@ -52,6 +53,7 @@ struct PublishArgs {
 
 struct SelectArgs {
   PoolArgs p;
+  int32_t block_shift;  // log2 of the positions per candidate block: 3, or 2/1/0 for a context shard
   const int32_t* blocks;
   int64_t blocks_stride;
   const int32_t* nvalid;
@@ -97,7 +99,31 @@ struct QProdArgs {
   int32_t* dev_err;
 };
 
+struct DcpKeysArgs {
+  const float* keys_local;  // [world][rows][local_stride]
+  int32_t world;
+  int64_t rank_stride, local_stride;
+  const int32_t* seq_len;  // global lengths
+  int32_t rows, max_len, skip_le_blocks;
+  float* keys;
+  int64_t keys_stride;
+  int32_t* dev_err;
+};
+
+struct DcpTopkArgs {
+  const int32_t* pos_local;  // [world][rows][local_stride]
+  const float* score_local;
+  int32_t world;
+  int64_t rank_stride, local_stride;
+  int32_t rows, topk;
+  int32_t* out_pos;
+  float* out_score;
+  int64_t out_stride;
+};
+
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
+cudaError_t launch_dcp_merge_keys(const DcpKeysArgs& a, cudaStream_t stream);
+cudaError_t launch_dcp_merge_topk(const DcpTopkArgs& a, cudaStream_t stream);
 cudaError_t launch_qprod(const QProdArgs& a, cudaStream_t stream);
 cudaError_t launch_tail(const TailArgs& a, cudaStream_t stream);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);

@@ -111,7 +111,7 @@ __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
   report(dev_err, kDevErrTimeout);
 }
 
-template <int R, int KV>
+template <int R, int KV, bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_amax8_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs a) {
   constexpr int N = 64 * R;                    // MMA N
@@ -465,10 +465,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int pos = t * kTileM + p;
         float v = pos < rlen ? score * kscale : -__int_as_float(0x7f800000);
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        if ((lane & 7) == 0 && pos < rlen) kp_row[t * (kTileM / kBlock)] = (pos >> 3) == nb - 1 ? __int_as_float(0x7f800000) : v;
+        if (kLocal) {
+          // a context shard's blocks of 1 << shift positions, no +inf pin (the
+          // merge across shards pins the global newest block)
+          const int bs = 1 << a.block_shift;
+          for (int o = 1; o < bs; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if ((lane & (bs - 1)) == 0 && pos < rlen) keys_row[pos >> a.block_shift] = v;
+        } else {
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          if ((lane & 7) == 0 && pos < rlen)
+            kp_row[t * (kTileM / kBlock)] = (pos >> 3) == nb - 1 ? __int_as_float(0x7f800000) : v;
+        }
       }
     }
     tseq += take;
@@ -499,11 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int R, int KV>
+template <int R, int KV, bool kLocal = false>
 cudaError_t launch_one(const CUtensorMap& tmap, const DenseArgs& a, int smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(dense_amax8_kernel<R, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(dense_amax8_kernel<R, KV, kLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dense_amax8_kernel<R, KV><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
+  dense_amax8_kernel<R, KV, kLocal><<<device_sm_count(), kThreads, smem, stream>>>(tmap, a);
   return cudaGetLastError();
 }
 
@@ -513,6 +523,8 @@ cudaError_t launch_dense_amax8(const DenseArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   const bool prefill = a.p.layout != kLayoutDecode;
+  if (a.block_shift != 3)  // a context shard's blocks (FP8 pages)
+    return prefill ? launch_one<3, kKvFp8, true>(tmap, a, smem, stream) : launch_one<1, kKvFp8, true>(tmap, a, smem, stream);
   if (a.p.kv_format == kKvMxfp4)
     return prefill ? launch_one<3, kKvMxfp4>(tmap, a, smem, stream) : launch_one<1, kKvMxfp4>(tmap, a, smem, stream);
   return prefill ? launch_one<3, kKvFp8>(tmap, a, smem, stream) : launch_one<1, kKvFp8>(tmap, a, smem, stream);

@@ -79,7 +79,8 @@ struct __align__(1024) Smem {
   uint8_t kv[kStages][kTileM * kDim];
   uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered
   uint8_t sf[2][512];                  // query scale factors staged for tcgen05.cp
-  // per candidate: (page << 7) | ((block & 7) << 4) | positions below L (1..8), or -1
+  // per candidate: (page << 10) | (8-position group in the page << 7) |
+  // (first position in the group << 4) | positions below L (1..8), or -1
   int32_t info[2][kMaxBlocks];
   int32_t bid[2][kMaxBlocks];  // the candidate block ids, for the top-k's output positions
   uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
@@ -141,7 +142,7 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int row, bool r
     bad = true;
   }
   if (bad) r.L = r.nv = 0;
-  r.nb = (r.L + kBlock - 1) / kBlock;
+  r.nb = (r.L + (1 << a.block_shift) - 1) >> a.block_shift;
   r.ntiles = (r.nv + kBlocksPerTile - 1) / kBlocksPerTile;
   return r;
 }
@@ -204,19 +205,25 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
       const int i = i0 + j * kPrepThreads + pid_t;
       blk[j] = i < r.nv ? brow[i] : -1;
     }
+    // candidate block blk covers positions blk << shift .. + (1 << shift) - 1
+    // (8 positions, or a context shard's 4, 2 or 1), inside one 8-position group
+    const int sh = a.block_shift;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) pid[j] = (blk[j] >= 0 && blk[j] < r.nb) ? pt[blk[j] >> 3] : -1;
+    for (int j = 0; j < kBatch; ++j) pid[j] = (blk[j] >= 0 && blk[j] < r.nb) ? pt[(blk[j] << sh) >> 6] : -1;
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int i = i0 + j * kPrepThreads + pid_t;
       if (i >= r.nv) continue;
       int v = -1;
-      if (blk[j] < 0 || blk[j] >= r.nb)
+      if (blk[j] < 0 || (blk[j] >= r.nb && sh == 3))
         report(a.p.dev_err, kDevErrBlock);
+      else if (blk[j] >= r.nb)
+        ;  // a context shard holds no position of this (global) block: empty
       else if (pid[j] < 0 || pid[j] >= a.p.num_pages)
         report(a.p.dev_err, kDevErrPage);
       else
-        v = (pid[j] << 7) | ((blk[j] & 7) << 4) | min(kBlock, r.L - blk[j] * kBlock);
+        v = (pid[j] << 10) | ((((blk[j] << sh) >> 3) & 7) << 7) | (((blk[j] << sh) & 7) << 4) |
+            min(1 << sh, r.L - (blk[j] << sh));
       sm.info[b][i] = v;
       sm.bid[b][i] = blk[j];
     }
@@ -605,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int blk = 0; blk < kTmaBlocks; ++blk) {
             const int vb = __shfl_sync(0xffffffffu, v, blk);
             if (vb >= 0)
-              tma_load_3d_elect(dst + blk * kBlockBytes, &tmap, 0, ((vb >> 4) & 7) * kBlock, vb >> 7,
+              tma_load_3d_elect(dst + blk * kBlockBytes, &tmap, 0, ((vb >> 7) & 7) * kBlock, vb >> 10,
                                 &sm.tk_full[kr.idx]);
           }
           ++issued;
@@ -619,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int v = slot < r.nv ? info[slot] : -1;
             if (v >= 0) {
               const uint8_t* src =
-                  a.p.k_pool + static_cast<int64_t>(v >> 7) * kPB + ((v >> 4) & 7) * kBlockBytes + lane * 16;
+                  a.p.k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
               if (kFp4) {
                 cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
               } else {
@@ -638,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int v = slot < r.nv ? info[slot] : -1;
               if (v >= 0)
                 cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
-                          a.p.k_pool + static_cast<int64_t>(v >> 7) * kPB + kPVB + 4 * (((v >> 4) & 7) * kBlock + (p & 7)));
+                          a.p.k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
             }
           }
           cp_async_arrive_noinc(&sm.k_full[kr.idx]);
@@ -688,7 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k > 0) {
         tmem_topk(
             sm, lane_base + kScoreCol + b * kMaxTiles, r.ntiles, k, kt,
-            [&](int rank, int t, int p) { out[rank] = sm.bid[b][t * kBlocksPerTile + (p >> 3)] * kBlock + (p & 7); },
+            [&](int rank, int t, int p) {
+              const int i = t * kBlocksPerTile + (p >> 3);
+              out[rank] = (sm.bid[b][i] << a.block_shift) + (p & 7) - ((sm.info[b][i] >> 4) & 7);
+            },
             osc != nullptr, [&](int rank, uint32_t u) { osc[rank] = order_key_inv(u); });
       }
       for (int i = max(k, 0) + kt; i < a.topk; i += kTopkThreads) {
@@ -731,13 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((tseq & 1) == static_cast<uint32_t>(e)) {
           const int slot = t * kBlocksPerTile + (p >> 3);
           const int v = slot < r.nv ? sm.info[b][slot] : -1;
-          const bool valid = v >= 0 && (p & 7) < (v & 15);
+          const int off = (v >> 4) & 7;
+          const bool valid = v >= 0 && (p & 7) >= off && (p & 7) < off + (v & 15);
           // this position's K scale, fetched now and used after the head sum
           // (MXFP4: 1, the scales are inside the MMA)
           float kscale = kFp4 ? 1.0f : 0.0f;
           if (!kFp4 && valid)
-            kscale = __ldg(reinterpret_cast<const float*>(a.p.k_pool + static_cast<int64_t>(v >> 7) * kPB + kPVB) +
-                           ((v >> 4) & 7) * kBlock + (p & 7));
+            kscale = __ldg(reinterpret_cast<const float*>(a.p.k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB) +
+                           ((v >> 7) & 7) * kBlock + (p & 7));
           if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
             ok = false;
             break;

@@ -301,3 +301,61 @@ def config_workload(cid: int, device="cpu", layers: int = 5, kv: int = KV_FP8) -
         device=device,
         kv=kv,
     )
+
+
+def _request_lengths(wl: Workload) -> list:
+    """The number of positions each request's pages must hold."""
+    L = wl.seq_len.cpu().tolist()
+    if wl.layout == LAYOUT_DECODE:
+        return L
+    if wl.layout == LAYOUT_PREFILL:
+        return [max(L) if L else 0]
+    starts = wl.req_start.cpu().tolist()
+    return [max(L[a:b]) if b > a else 0 for a, b in zip(starts[:-1], starts[1:])]
+
+
+def shard_workload(wl: Workload, world: int) -> list:
+    """The ``world`` context shards of an FP8 workload, interleave 1: global
+    position s of a request lives on shard s % world at local position
+    s // world (vLLM sparse_attn_indexer.py, two-level candidate filtering
+    under DCP).  Each shard gets its own pools and page table holding its
+    positions, and the local lengths; queries and weights are replicated.
+    Pure data movement (the sharded cache layout), no arithmetic of the
+    method."""
+    assert wl.kv == KV_FP8
+    dev = wl.seq_len.device
+    L = wl.seq_len.to(torch.int64)
+    req_len = _request_lengths(wl)
+    pt = wl.page_table.to(torch.int64)
+    shards = []
+    for r in range(world):
+        local_len = [max(0, (n - r + world - 1) // world) for n in req_len]
+        pages = [(n + PAGE - 1) // PAGE for n in local_len]
+        num_pages = max(sum(pages), 1)
+        lpt = torch.full((len(pages), max(max(pages) if pages else 0, 1)), -1, dtype=torch.int32)
+        src_page, src_slot, dst_page, dst_slot = [], [], [], []
+        off = 0
+        for q, (n, np_) in enumerate(zip(local_len, pages)):
+            lpt[q, :np_] = torch.arange(off, off + np_, dtype=torch.int32)
+            if n:
+                j = torch.arange(n, device=dev)
+                s = j * world + r
+                src_page.append(pt[q].to(dev)[s // PAGE])
+                src_slot.append(s % PAGE)
+                dst_page.append(off + j // PAGE)
+                dst_slot.append(j % PAGE)
+            off += np_
+        layers = []
+        for l in wl.layers:
+            pool = torch.zeros(num_pages, PAGE_BYTES, dtype=torch.uint8, device=dev)
+            if src_page:
+                sp, ss, dp, ds = (torch.cat(x) for x in (src_page, src_slot, dst_page, dst_slot))
+                vals = l.k_pool[:, :PAGE_VALUE_BYTES].reshape(-1, PAGE, D)
+                scl = l.k_pool[:, PAGE_VALUE_BYTES:].reshape(-1, PAGE, 4)
+                pool[:, :PAGE_VALUE_BYTES].view(-1, PAGE, D)[dp, ds] = vals[sp, ss]
+                pool[:, PAGE_VALUE_BYTES:].view(-1, PAGE, 4)[dp, ds] = scl[sp, ss]
+            layers.append(Layer(l.q_fp4, l.q_sf, l.w, pool))
+        local = torch.clamp(L - r + world - 1, min=0) // world
+        shards.append(Workload(f"{wl.name}_shard{r}of{world}", wl.layout, local.to(torch.int32).to(dev),
+                               lpt.to(dev), layers, wl.topk_blocks, wl.topk, wl.req_start))
+    return shards
