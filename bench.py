@@ -199,26 +199,24 @@ def time_steps(step, steps, warmup, flush, stream, dense_events=True):
     return out
 
 
-def e2e_time(step, host_inputs, steps, stream):
-    """The same step through the C ABI with host buffers: pinned host -> device
-    copies of the step's inputs, the step, and device -> host of its results,
-    all inside the timed region."""
-    wl = step.wl
-    dev_tensors = [wl.seq_len, wl.page_table] + [t for l in wl.layers for t in (l.q_fp4, l.q_sf, l.w, l.k_pool)]
-    outs = [step.pos, step.blocks, step.nvalid]
+def e2e_time(step, steps, stream):
+    """The same step through the library's public API with host buffers:
+    IndexerStep.run_host copies the step's inputs from pinned host memory
+    and its results (published blocks, every layer's positions) back to
+    pinned host memory, overlapping the copies with the kernels; all of it
+    inside the timed region."""
+    shared, layers = step.device_inputs()
+    host_shared = [t.cpu().pin_memory() for t in shared]
+    host_layers = [[t.cpu().pin_memory() for t in l] for l in layers]
+    outs = [step.blocks, step.nvalid] + [step.pos[j] for j in range(len(layers))]
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    h2d = sum(t.numel() * t.element_size() for t in host_shared + [x for l in host_layers for x in l])
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     times = []
     for _ in range(steps + 1):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for d, h in zip(dev_tensors, host_inputs):
-                d.copy_(h, non_blocking=True)
-            step.run(stream)
-            for h, o in zip(host_out, outs):
-                h.copy_(o, non_blocking=True)
+        step.run_host(host_shared, host_layers, host_out, stream)
         stream.synchronize()
         times.append((time.perf_counter() - t0) * 1e3)
     return times[1:], h2d, d2h
@@ -316,9 +314,7 @@ def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0, wl=None):
     res = {"cid": cid, "wl": wl, "step": step, "t_step": times["step"], "t_dense": times["dense"],
            "t_select": times["select"], "t_publish": times["publish"], "launches": step.launches()}
     if e2e:
-        host = [t.cpu().pin_memory() for t in [wl.seq_len, wl.page_table] +
-                [x for l in wl.layers for x in (l.q_fp4, l.q_sf, l.w, l.k_pool)]]
-        res["e2e"] = e2e_time(step, host, max(2, min(steps, 5)), stream)
+        res["e2e"] = e2e_time(step, max(2, min(steps, 5)), stream)
     return res
 
 

@@ -579,3 +579,33 @@ def test_dcp_step_equals_unsharded_step_bitwise(ci, world, case):
     nb = (wl.seq_len.numpy() + 7) // 8
     for t in np.nonzero(nb > min(wl.topk_blocks, wl.topk + 1))[0]:
         np.testing.assert_array_equal(b["keys"][t, : nb[t]].view(np.uint32), a["keys"][t, : nb[t]].view(np.uint32))
+
+
+@needs_cuda
+@pytest.mark.parametrize("case", ["decode", "prefill"])
+def test_run_host_moves_the_same_results(ci, case):
+    """IndexerStep.run_host (pinned host in, pinned host out, copies overlapped
+    with the kernels) returns exactly what run() leaves on the device."""
+    from two_level_sparse_gb300.step import IndexerStep
+
+    if case == "decode":  # fewer rows than SMs: the selects run side by side
+        wl = synth.make_workload("rh", synth.LAYOUT_DECODE, [5000, 5001, 4096, 4095, 65], 64, seed=41, topk=40)
+    else:
+        wl = synth.make_workload("rh", synth.LAYOUT_PREFILL, [3000 + i for i in range(200)], 64, seed=42)
+    dev = wl.to("cuda")
+    step = IndexerStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    want = [step.blocks.cpu(), step.nvalid.cpu()] + [step.pos[j].cpu() for j in range(len(wl.layers))]
+    shared, layers = step.device_inputs()
+    host_shared = [t.cpu().pin_memory() for t in shared]
+    host_layers = [[t.cpu().pin_memory() for t in l] for l in layers]
+    for t in shared + [x for l in layers for x in l]:
+        t.zero_()  # the inputs must come from the host copies
+    for j in range(len(wl.layers)):
+        step.pos[j].fill_(-7)
+    host_out = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in want]
+    step.run_host(host_shared, host_layers, host_out, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    for got, exp in zip(host_out, want):
+        assert torch.equal(got, exp)

@@ -110,6 +110,71 @@ class IndexerStep:
                 main.wait_event(joined)
             mark("select")
 
+    def device_inputs(self):
+        """The step's input tensors, shared ones first, then layer by layer."""
+        wl = self.wl
+        shared = [wl.seq_len, wl.page_table] + ([] if wl.req_start is None else [wl.req_start])
+        return shared, [[l.q_fp4, l.q_sf, l.w, l.k_pool] for l in wl.layers]
+
+    def run_host(self, host_shared, host_layers, host_out, stream=None):
+        """The step from pinned host inputs to pinned host outputs.
+
+        ``host_shared`` / ``host_layers`` mirror ``device_inputs()``;
+        ``host_out`` receives (blocks, nvalid, pos[layer] ...).  The shared
+        and source-layer inputs are copied first; the consumers' inputs copy on
+        a second stream while the source is scored; the published blocks and
+        each layer's positions copy back while later layers run.  All copies
+        finish before ``stream`` does."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.dev_err.device)
+        if not hasattr(self, "_copy"):
+            self._copy = torch.cuda.Stream(device=self.dev_err.device)
+        cp = self._copy
+        shared, layers = self.device_inputs()
+        start = torch.cuda.Event()
+        start.record(main)  # the previous step on `main` is done with these buffers once this passes
+        with torch.cuda.stream(main):
+            for d, h in zip(shared + layers[0], host_shared + host_layers[0]):
+                d.copy_(h, non_blocking=True)
+        cp.wait_event(start)
+        ready = []
+        with torch.cuda.stream(cp):
+            for dl, hl in zip(layers[1:], host_layers[1:]):
+                for d, h in zip(dl, hl):
+                    d.copy_(h, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cp)
+                ready.append(ev)
+        outs = [self.blocks, self.nvalid] + [self.pos[j] for j in range(len(layers))]
+
+        def mark(name, _state={"sel": 0}):
+            if name == "publish":
+                # consumers need their inputs; copy the published table back
+                for ev in ready:
+                    main.wait_event(ev)
+                done = torch.cuda.Event()
+                done.record(main)
+                cp.wait_event(done)
+                with torch.cuda.stream(cp):
+                    host_out[0].copy_(outs[0], non_blocking=True)
+                    host_out[1].copy_(outs[1], non_blocking=True)
+            elif name == "select":
+                j = _state["sel"]
+                _state["sel"] += 1
+                done = torch.cuda.Event()
+                done.record(main)
+                cp.wait_event(done)
+                with torch.cuda.stream(cp):
+                    if self.concurrent:  # all layers joined into `main` at once
+                        for k in range(len(layers)):
+                            host_out[2 + k].copy_(outs[2 + k], non_blocking=True)
+                    else:
+                        host_out[2 + j].copy_(outs[2 + j], non_blocking=True)
+
+        self.run(main, mark=mark)
+        end = torch.cuda.Event()
+        end.record(cp)
+        main.wait_event(end)
+
     def outputs_numpy(self):
         out = dict(keys=self.keys.cpu().numpy(), blocks=self.blocks.cpu().numpy(), nvalid=self.nvalid.cpu().numpy(),
                    blocks_src=self.blocks_src.cpu().numpy(), nvalid_src=self.nvalid_src.cpu().numpy(),
