@@ -597,12 +597,12 @@ def rooflines(a, b):
 # at full size (one-pass metrics), with the hash of the kernel's sources; a
 # figure is reported only while the sources still match.
 RECORDED_TRAFFIC = {
-    # mean of the five launches of a step (source 170.5 MB, consumers 273-277 MB)
-    "select_kernel": {"bytes_per_launch": 253.7e6, "sources": ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
-                      "sha256": "3ad6bad76c6f03ee37e231ff47a45fb0619976bd4acc3c067ecc28d9fef21e21"},
-    # 130.4 MB read (pool, queries) + 2038.1 MB written (keys)
-    "dense_amax8_kernel": {"bytes_per_launch": 2168.4e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
-                           "sha256": "749f7e6e4d807ccc285221b9941b1d085ab43c55effdc581537489922552dee0"},
+    # mean of the five launches of a step (source 171.3 MB, consumers 272.6-274.1 MB)
+    "select_kernel": {"bytes_per_launch": 252.8e6, "sources": ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+                      "sha256": "44ead527b3179d632a1481cd62af6d6c3bfd1472c94b572c32ff229361902eee"},
+    # 129.2 MB read (pool, queries) + 2038.0 MB written (keys)
+    "dense_amax8_kernel": {"bytes_per_launch": 2167.2e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+                           "sha256": "7405a49da0a8f885945c6f8d05467c7ce6d7474b23e8d87d4e70fbc3111e2516"},
 }
 
 
