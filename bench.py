@@ -199,6 +199,24 @@ def time_steps(step, steps, warmup, flush, stream, dense_events=True):
     return out
 
 
+def graph_step_ms(step, steps, stream, flush):
+    """Mean device time of the step replayed as a CUDA graph (L2 flushed
+    before every replay)."""
+    graph = step.capture(stream)
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                ms.append(e0.elapsed_time(e1))
+    return statistics.mean(ms)
+
+
 def e2e_time(step, steps, stream):
     """The same step through the library's public API with host buffers:
     IndexerStep.run_host copies the step's inputs from pinned host memory
@@ -521,15 +539,18 @@ def main():
     if not args.no_secondary:
         del head
         torch.cuda.empty_cache()
-        for cid in (2, 1):
+        for cid in (2, 1, 0):
             r = measure(cid, max(3, args.steps // 2), 3, stream, flush)
             mst = statistics.mean(r["t_step"])
             msd = statistics.mean(r["t_dense"])
+            msg = graph_step_ms(r["step"], max(3, args.steps // 2), stream, flush)
             f, b, _ = algorithmic_counts(r["wl"])
             rows = r["wl"].rows
             secondary.append({
                 "metric": "decode rows/s", "workload": r["wl"].name, "value": world * rows / (mst * 1e-3),
                 "unit": "rows/s", "ms_per_step": mst, "dense_ms": msd,
+                "graph": {"ms_per_step": msg, "rows_per_s": world * rows / (msg * 1e-3),
+                          "note": "the same step replayed as a CUDA graph"},
                 "dense_roofline": {"bound": "hbm", "achieved": b / (msd * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                                    "unit": "GB/s", "frac": b / (msd * 1e-3) / 1e9 / peaks["hbm_gbs"]},
                 "dev_err": int(r["step"].dev_err.item()),

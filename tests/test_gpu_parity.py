@@ -609,3 +609,27 @@ def test_run_host_moves_the_same_results(ci, case):
     torch.cuda.synchronize()
     for got, exp in zip(host_out, want):
         assert torch.equal(got, exp)
+
+
+@needs_cuda
+@pytest.mark.parametrize("cid", [0])
+def test_graph_replay_equals_eager_step(ci, cid):
+    """The step captured as a CUDA graph (side streams included) reproduces the
+    eager step's outputs."""
+    from two_level_sparse_gb300.step import IndexerStep
+
+    wl = synth.config_workload(cid, device="cuda")
+    step = IndexerStep(wl, with_scores=True)
+    s = torch.cuda.Stream()
+    step.run(s)
+    torch.cuda.synchronize()
+    want = step.outputs_numpy()
+    g = step.capture(s)
+    step.pos.fill_(-9)
+    step.blocks.fill_(-9)
+    g.replay()
+    torch.cuda.synchronize()
+    got = step.outputs_numpy()
+    for k in ("blocks", "nvalid", "pos"):
+        np.testing.assert_array_equal(got[k], want[k], err_msg=k)
+    np.testing.assert_array_equal(got["score"].view(np.uint32), want["score"].view(np.uint32))

@@ -110,6 +110,17 @@ class IndexerStep:
                 main.wait_event(joined)
             mark("select")
 
+    def capture(self, stream):
+        """The step captured as a CUDA graph on ``stream`` (same buffers):
+        replaying it enqueues every launch, the side streams' fork and join
+        included, without per-launch host work -- what small decode batches,
+        bound by launch latency, need.  Run the step once before capturing
+        (the first launches set kernel attributes)."""
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self.run(stream)
+        return graph
+
     def device_inputs(self):
         """The step's input tensors, shared ones first, then layer by layer."""
         wl = self.wl
