@@ -633,3 +633,15 @@ def test_graph_replay_equals_eager_step(ci, cid):
     for k in ("blocks", "nvalid", "pos"):
         np.testing.assert_array_equal(got[k], want[k], err_msg=k)
     np.testing.assert_array_equal(got["score"].view(np.uint32), want["score"].view(np.uint32))
+
+
+@needs_cuda
+def test_maximum_sizes(ci):
+    """The largest supported sizes in one step: a row of 393216 positions
+    (the publish limit), 2176 candidate blocks per consumer row (the select
+    limit), top-2048 positions (the top-k limit, so the source selects within
+    its top 2049 blocks), beside a 17-position row."""
+    wl = synth.make_workload("max", synth.LAYOUT_DECODE, [393216, 17], 2176, seed=55, topk=2048)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    assert_ok(compare.check_step(wl, step.outputs_numpy()))
