@@ -488,6 +488,8 @@ def main():
                     help="keep only the last ROWS rows of the headline chunk (a smaller case for profilers)")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "mxfp4"],
                     help="index-K page format of the headline chunk (the reported metric is defined on fp8)")
+    ap.add_argument("--only", default=None, choices=["qprod", "varlen", "mxfp4", "dcp"],
+                    help="run one secondary workload alone and print its line (a small command for profilers)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -509,6 +511,17 @@ def main():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+
+    if args.only is not None:
+        steps = max(1, args.steps)
+        one = {"qprod": lambda: measure_qprod(steps, stream, flush, peaks),
+               "varlen": lambda: measure_varlen(steps, stream, flush, world),
+               "mxfp4": lambda: measure_mxfp4(steps, stream, flush, world, peaks),
+               "dcp": lambda: measure_dcp(steps, stream, flush, 2)}[args.only]()
+        emit_line(one, rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
 
     barrier()
     with ClockSampler(local) as clk:

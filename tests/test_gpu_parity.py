@@ -341,6 +341,7 @@ def run_tail(ci, rows_per_req, tail_lens, K, cap, seed):
     ((4, 4, 4), (0, -3, 4), 2048, 5),                     # nothing kept, negative length, spare capacity padded
     ((1,) * 4096, tuple(i % 2 for i in range(4096)), 64, 3),  # the most requests: every other one kept
     ((16384,), (4096,), 2048, 0),                         # one long request, the tail a quarter of it
+    ((3, 5, 2), (2, 4, 9), 13, 2),                        # rows of 13 ids: 4-byte copies, no 16-byte path
 ])
 def test_prefill_tail_gathers_tail_rows_bit_exact(ci, rows_per_req, tail_lens, K, extra):
     starts, blocks, nvalid, _, _, _, _, _ = run_tail(ci, rows_per_req, tail_lens, K, 0, seed=11)

@@ -34,16 +34,18 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 constexpr int kHeadsPerWarp = 8;  // loads of eight heads in flight per warp before any is processed
 
-// Exact ceil(log2(max(amax, 1e-10) * (1 / vmax))).
-__device__ __forceinline__ int scale_exp(float amax, float inv_vmax) {
-  const uint32_t u = __float_as_uint(__fmul_rn(fmaxf(amax, 1e-10f), inv_vmax));
-  return static_cast<int>((u >> 23) & 0xFFu) - 127 + ((u & 0x7FFFFFu) != 0u);
+// The biased scale exponent 127 + ceil(log2(max(amax, 1e-10) * (1 / vmax))),
+// which is also the ue8m0 code of the scale.  For a positive normal float,
+// adding 0x7FFFFF to its bits carries into the exponent field exactly when
+// the mantissa is nonzero, so the field of the sum is the ceiling.  (The
+// product lies in [2^-43, 2^126]: amax is at least 1e-10 and at most the
+// largest bf16.)
+__device__ __forceinline__ uint32_t scale_code(float amax, float inv_vmax) {
+  return (__float_as_uint(__fmul_rn(fmaxf(amax, 1e-10f), inv_vmax)) + 0x7FFFFFu) >> 23;
 }
-// 2^k from its bits, for -126 <= k <= 127 (the scale exponents here lie in
-// [-33, 126]: amax is at least 1e-10 and at most the largest bf16).
-__device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
-// x * 2^-e, exact (a power-of-two scaling).
-__device__ __forceinline__ float unscale(float x, int e) { return __fmul_rn(x, pow2i(-e)); }
+// The scale 2^(code - 127) and its inverse, from bits (both exact).
+__device__ __forceinline__ float scale_of(uint32_t code) { return __uint_as_float(code << 23); }
+__device__ __forceinline__ float inv_scale_of(uint32_t code) { return __uint_as_float((254u - code) << 23); }
 // Two fp32 values -> one byte of e2m1 codes, `lo` in the low nibble.
 __device__ __forceinline__ uint8_t e2m1_pair(float lo, float hi) {
   return static_cast<uint8_t>(__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest));
@@ -102,16 +104,17 @@ __device__ __forceinline__ void qprod_head(const QProdArgs& a, int64_t gw, int m
     float amax = fmaxf(ma, mb);  // over the head's 16 lanes
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const int e = scale_exp(amax, 1.0f / 448.0f);
+    const uint32_t code = scale_code(amax, 1.0f / 448.0f);
+    const float inv = inv_scale_of(code);
     uint32_t pa = 0, pb = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      pa |= static_cast<uint32_t>(e4m3(fminf(fmaxf(unscale(v[j], e), -448.0f), 448.0f))) << (8 * j);
-      pb |= static_cast<uint32_t>(e4m3(fminf(fmaxf(unscale(y[j], e), -448.0f), 448.0f))) << (8 * j);
+      pa |= static_cast<uint32_t>(e4m3(fminf(fmaxf(__fmul_rn(v[j], inv), -448.0f), 448.0f))) << (8 * j);
+      pb |= static_cast<uint32_t>(e4m3(fminf(fmaxf(__fmul_rn(y[j], inv), -448.0f), 448.0f))) << (8 * j);
     }
     *reinterpret_cast<uint32_t*>(a.q_out + gw * kDim + 4 * m) = pa;
     *reinterpret_cast<uint32_t*>(a.q_out + gw * kDim + 64 + 4 * m) = pb;
-    if (m == 0) a.w_out[gw] = __fmul_rn(__fmul_rn(__fmul_rn(w, pow2i(e)), a.softmax_scale), a.head_scale);
+    if (m == 0) a.w_out[gw] = __fmul_rn(__fmul_rn(__fmul_rn(w, scale_of(code)), a.softmax_scale), a.head_scale);
   } else {
     // block maxima over lane octets, both blocks in one word: every value is
     // a bf16, so |max| is the upper half of its fp32 bits, and for
@@ -119,9 +122,9 @@ __device__ __forceinline__ void qprod_head(const QProdArgs& a, int64_t gw, int m
     uint32_t pm = __byte_perm(__float_as_uint(ma), __float_as_uint(mb), 0x7632);
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) pm = __vmaxu2(pm, __shfl_xor_sync(0xffffffffu, pm, off));
-    const int ea = scale_exp(__uint_as_float(pm << 16), 1.0f / 6.0f);
-    const int eb = scale_exp(__uint_as_float(pm & 0xFFFF0000u), 1.0f / 6.0f);
-    const float sa = pow2i(-ea), sb = pow2i(-eb);  // exact power-of-two scalings
+    const uint32_t ka = scale_code(__uint_as_float(pm << 16), 1.0f / 6.0f);
+    const uint32_t kb = scale_code(__uint_as_float(pm & 0xFFFF0000u), 1.0f / 6.0f);
+    const float sa = inv_scale_of(ka), sb = inv_scale_of(kb);
     const uint32_t ca = e2m1_pair(__fmul_rn(v[0], sa), __fmul_rn(v[1], sa)) |
                         (static_cast<uint32_t>(e2m1_pair(__fmul_rn(v[2], sa), __fmul_rn(v[3], sa))) << 8);
     const uint32_t cb = e2m1_pair(__fmul_rn(y[0], sb), __fmul_rn(y[1], sb)) |
@@ -129,7 +132,7 @@ __device__ __forceinline__ void qprod_head(const QProdArgs& a, int64_t gw, int m
     *reinterpret_cast<uint16_t*>(a.q_out + gw * (kDim / 2) + 2 * m) = static_cast<uint16_t>(ca);
     *reinterpret_cast<uint16_t*>(a.q_out + gw * (kDim / 2) + 32 + 2 * m) = static_cast<uint16_t>(cb);
     // ue8m0 codes: byte j of the head's word = block j
-    const uint32_t cw = static_cast<uint32_t>(ea + 127) | (static_cast<uint32_t>(eb + 127) << 16);
+    const uint32_t cw = ka | (kb << 16);
     const uint32_t other = __shfl_xor_sync(0xffffffffu, cw, 8);  // blocks 1 and 3 (lane 8 of the half)
     if (m == 0) {
       *reinterpret_cast<uint32_t*>(a.q_sf + gw * 4) = cw | (other << 8);

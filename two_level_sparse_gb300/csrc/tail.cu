@@ -14,7 +14,7 @@
 namespace ci {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;  // a 2048-id row is two 16-byte copies per thread
 constexpr int kPer = kMaxReq / kThreads;
 
 __global__ void __launch_bounds__(kThreads) tail_kernel(const TailArgs a) {
@@ -61,6 +61,10 @@ __global__ void __launch_bounds__(kThreads) tail_kernel(const TailArgs a) {
     if (total > a.out_cap) report(a.dev_err, kDevErrReq);
   }
   const int n = min(total, a.out_cap);
+  // 16-byte copies when every row of both tables starts on a 16-byte boundary
+  const bool vec = ((a.topk_blocks | a.blocks_stride | a.out_blocks_stride) & 3) == 0 &&
+                   ((reinterpret_cast<uintptr_t>(a.blocks) | reinterpret_cast<uintptr_t>(a.out_blocks)) & 15) == 0;
+  const int nvec = vec ? a.topk_blocks / 4 : 0;
   for (int o = blockIdx.x; o < a.out_cap; o += gridDim.x) {
     int src = -1;
     if (o < n) {
@@ -77,9 +81,12 @@ __global__ void __launch_bounds__(kThreads) tail_kernel(const TailArgs a) {
     int32_t* ob = a.out_blocks + static_cast<int64_t>(o) * a.out_blocks_stride;
     if (src >= 0) {
       const int32_t* ib = a.blocks + static_cast<int64_t>(src) * a.blocks_stride;
-      for (int i = tid; i < a.topk_blocks; i += kThreads) ob[i] = ib[i];
+      for (int i = tid; i < nvec; i += kThreads) reinterpret_cast<int4*>(ob)[i] = reinterpret_cast<const int4*>(ib)[i];
+      for (int i = 4 * nvec + tid; i < a.topk_blocks; i += kThreads) ob[i] = ib[i];
     } else {
-      for (int i = tid; i < a.topk_blocks; i += kThreads) ob[i] = 0x7FFFFFFF;
+      const int4 pad = make_int4(0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF);
+      for (int i = tid; i < nvec; i += kThreads) reinterpret_cast<int4*>(ob)[i] = pad;
+      for (int i = 4 * nvec + tid; i < a.topk_blocks; i += kThreads) ob[i] = 0x7FFFFFFF;
     }
     if (tid == 0) {
       a.out_row[o] = src;
@@ -91,7 +98,9 @@ __global__ void __launch_bounds__(kThreads) tail_kernel(const TailArgs a) {
 }  // namespace
 
 cudaError_t launch_tail(const TailArgs& a, cudaStream_t stream) {
-  const int grid = max(1, min(a.out_cap, 4 * device_sm_count()));
+  // one output row per CTA (several rounds only past 64 K rows): the rows'
+  // copies all start at once instead of one after another in each CTA
+  const int grid = max(1, min(a.out_cap, 65536));
   tail_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
