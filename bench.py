@@ -601,7 +601,8 @@ def main():
              "peak_source": f"{peak_src} hbm_gbs",
              "bytes_per_launch": sel_bytes / n_select, "launches_per_step": n_select,
              "ms_per_launch": ms_select / n_select, "ms_per_step": ms_select,
-             "note": "candidate K gathered per launch (132 B per position) / mean launch time; "
+             "note": "candidate K gathered per launch (132 B per position) / mean launch time (the five "
+                     "launches run on side streams and overlap at their edges: the select phase / 5); "
                      "for a prefill chunk the 34.6 MB pool per layer is L2-resident"}),
         "kernel_ms": {"dense": ms_dense, "publish": ms_publish, "select": ms_select},
         "e2e": {"value": e2e_val / world, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -658,7 +659,7 @@ def recorded_traffic(kernel):
 
 
 def head_launches(steps, world):
-    # per step: dense 1 + publish 1 (K and P + 1 together) + select 5
+    # per step of the 16384-row chunk: dense 1 + publish 1 (K and P + 1 together) + select 5 (one per layer)
     return steps * 7
 
 

@@ -28,7 +28,8 @@
  *   level two, once per layer (the source itself and each consumer):
  *     ci_select_sparse       scores only the positions inside a row's
  *                            published blocks and returns its top-k positions,
- *                            ascending, -1 padded.
+ *                            ascending, -1 padded;
+ *     ci_select_sparse_layers  the same for several layers in one launch.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -253,6 +254,31 @@ CI_API int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const flo
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
                      int32_t block_positions, int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride,
                      int32_t* dev_err, void* stream);
+
+/*
+ * Level two for several layers in one launch: layer l (0 <= l < num_layers
+ * <= 8) is exactly ci_select_sparse with q_fp4[l], q_sf[l], w[l], k_pool[l],
+ * blocks[l], blocks_stride[l], nvalid[l], max_blocks[l], out_pos[l] and
+ * out_score[l] (out_score itself may be NULL: no scores for any layer; or
+ * out_score[l] NULL: none for layer l).  The page table, layout, lengths,
+ * pool format and size, block_positions, topk and out_stride are shared:
+ * the layers of one step (the source with its own top-(P+1) blocks and every
+ * consumer with the published ones; PR #40352, Design, "Level two") read
+ * their own pools through the same pages.  The per-layer arguments are HOST
+ * arrays of num_layers entries, each entry a device pointer (or, for
+ * blocks_stride and max_blocks, a value).  One persistent grid works through
+ * the (layer, row) pairs layer by layer, so a layer's last rows overlap the
+ * next layer's first and small batches fill every SM.  Each layer's checks
+ * are ci_select_sparse's; CI_ERR_RANGE if num_layers is outside 1..8.
+ */
+CI_API int ci_select_sparse_layers(int32_t num_layers, const uint8_t* const* q_fp4, const uint8_t* const* q_sf,
+                                   const float* const* w, const uint8_t* const* k_pool, int64_t num_pages,
+                                   int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages,
+                                   int32_t layout, const int32_t* req_row_start, const int32_t* seq_len, int32_t rows,
+                                   int32_t max_len, const int32_t* const* blocks, const int64_t* blocks_stride,
+                                   const int32_t* const* nvalid, const int32_t* max_blocks, int32_t block_positions,
+                                   int32_t topk, int32_t* const* out_pos, float* const* out_score, int64_t out_stride,
+                                   int32_t* dev_err, void* stream);
 
 /*
  * The exchange steps of a context-sharded indexer with W = world shards

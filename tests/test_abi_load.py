@@ -30,7 +30,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(
         ["ci_dcp_merge_keys", "ci_dcp_merge_topk", "ci_prefill_tail", "ci_publish_blocks", "ci_publish_blocks2",
-         "ci_q_rope_quant", "ci_score_dense_amax8", "ci_select_sparse", "ci_strerror", "ci_version"])
+         "ci_q_rope_quant", "ci_score_dense_amax8", "ci_select_sparse", "ci_select_sparse_layers", "ci_strerror",
+         "ci_version"])
 
 
 def test_library_exports_every_declared_symbol(ci):
@@ -41,7 +42,7 @@ def test_library_exports_every_declared_symbol(ci):
 
 
 def test_status_names(ci):
-    assert ci.version() == 300
+    assert ci.version() == 301
     assert ci.strerror(0) == "ok"
     for code in ci.CI_ERR:
         assert ci.strerror(code) != "unknown status"
@@ -180,6 +181,32 @@ def test_select_host_checks(ci):
     bad = list(ok_args)
     bad[18] = 16  # block size other than 8, 4, 2, 1
     assert f(*bad) == -4
+
+
+def test_select_layers_host_checks(ci):
+    f = ci.lib.ci_select_sparse_layers
+    n = 2
+    ptrs = (ctypes.c_void_p * n)(0x1000, 0x2000)
+    i64 = (ctypes.c_int64 * n)(16, 16)
+    i32 = (ctypes.c_int32 * n)(16, 16)
+
+    def args(num_layers=n, mb=i32, outs=ptrs, rows=2, topk=8, kv=0):
+        return [num_layers, ptrs, ptrs, ptrs, ptrs, 1, kv, P, 2, 1, 0, N, P, rows, 64, ptrs, i64, ptrs, mb, 8, topk,
+                outs, N, 8, N, N]
+
+    assert f(*args(rows=0)) == 0  # nothing to do
+    assert f(*args(num_layers=0)) == -4
+    assert f(*args(num_layers=9)) == -4
+    assert f(*args(mb=(ctypes.c_int32 * n)(16, 5000))) == -4  # the second layer's max_blocks too large
+    assert f(*args(outs=(ctypes.c_void_p * n)(0x1000, None))) == -1  # the second layer has no output
+    assert f(*args(topk=0)) == -4
+    assert f(*args(kv=3)) == -5
+    bad = args()
+    bad[1] = N  # no q array
+    assert f(*bad) == -1
+    bad = args()
+    bad[23] = 4  # out stride < topk
+    assert f(*bad) == -2
 
 
 def test_dcp_merge_host_checks(ci):

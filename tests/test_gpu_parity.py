@@ -584,12 +584,60 @@ def test_dcp_step_equals_unsharded_step_bitwise(ci, world, case):
 
 @needs_cuda
 @pytest.mark.parametrize("case", ["decode", "prefill"])
+def test_select_layers_equals_one_launch_per_layer(ci, case):
+    """One ci_select_sparse_layers launch over every layer (the source with
+    its top-(P+1) blocks, the consumers with the published K) writes bit for
+    bit what one ci_select_sparse launch per layer writes, scores for some
+    layers and not others included."""
+    from two_level_sparse_gb300.step import IndexerStep
+
+    if case == "decode":  # 5 x 7 (layer, row) units on a grid of 35 CTAs
+        wl = synth.make_workload("sl", synth.LAYOUT_DECODE, [9000, 3001, 20000, 64, 4096, 700, 15000], 96, seed=51,
+                                 topk=60)
+    else:  # 5 x 300 units on one CTA per SM: layer boundaries inside every CTA's sequence
+        wl = synth.make_workload("sl", synth.LAYOUT_PREFILL, [2500 + 7 * i for i in range(300)], 48, seed=52, topk=40)
+    dev = wl.to("cuda")
+    step = IndexerStep(dev, with_scores=True)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) == 0
+    for j, layer in enumerate(dev.layers):
+        blocks, nvalid, mb = (step.blocks_src, step.nvalid_src, step.Kp) if j == 0 else (step.blocks, step.nvalid,
+                                                                                        step.K)
+        pos = torch.full_like(step.pos[j], -9)
+        score = torch.full_like(step.score[j], 7.0) if j % 2 == 0 else None
+        ci.ci_select_sparse(layer.q_fp4, layer.q_sf, layer.w, layer.k_pool, dev.page_table, dev.layout, dev.seq_len,
+                            dev.max_len, blocks, nvalid, mb, step.P, pos, score, dev_err=step.dev_err)
+        torch.cuda.synchronize()
+        assert torch.equal(pos, step.pos[j]), j
+        if score is not None:
+            assert torch.equal(score.view(torch.int32), step.score[j].view(torch.int32)), j
+    # scores for layer 1 only, positions for all: the other layers' score rows stay untouched
+    out_pos = torch.full_like(step.pos, -9)
+    out_score = torch.full_like(step.score, 7.0)
+    layers = []
+    for j, layer in enumerate(dev.layers):
+        blocks, nvalid, mb = (step.blocks_src, step.nvalid_src, step.Kp) if j == 0 else (step.blocks, step.nvalid,
+                                                                                        step.K)
+        layers.append(dict(q_fp4=layer.q_fp4, q_sf=layer.q_sf, w=layer.w, k_pool=layer.k_pool, blocks=blocks,
+                           nvalid=nvalid, max_blocks=mb, out_pos=out_pos[j], out_score=out_score[j] if j == 1 else None))
+    ci.ci_select_sparse_layers(layers, dev.page_table, dev.layout, dev.seq_len, dev.max_len, step.P,
+                               dev_err=step.dev_err)
+    torch.cuda.synchronize()
+    assert torch.equal(out_pos, step.pos)
+    assert torch.equal(out_score[1].view(torch.int32), step.score[1].view(torch.int32))
+    assert bool((out_score[0] == 7.0).all()) and bool((out_score[2:] == 7.0).all())
+    assert int(step.dev_err.item()) == 0
+
+
+@needs_cuda
+@pytest.mark.parametrize("case", ["decode", "prefill"])
 def test_run_host_moves_the_same_results(ci, case):
     """IndexerStep.run_host (pinned host in, pinned host out, copies overlapped
     with the kernels) returns exactly what run() leaves on the device."""
     from two_level_sparse_gb300.step import IndexerStep
 
-    if case == "decode":  # fewer rows than SMs: the selects run side by side
+    if case == "decode":  # fewer rows than SMs: the select launch spreads every layer's rows over the SMs
         wl = synth.make_workload("rh", synth.LAYOUT_DECODE, [5000, 5001, 4096, 4095, 65], 64, seed=41, topk=40)
     else:
         wl = synth.make_workload("rh", synth.LAYOUT_PREFILL, [3000 + i for i in range(200)], 64, seed=42)
@@ -615,8 +663,7 @@ def test_run_host_moves_the_same_results(ci, case):
 @needs_cuda
 @pytest.mark.parametrize("cid", [0])
 def test_graph_replay_equals_eager_step(ci, cid):
-    """The step captured as a CUDA graph (side streams included) reproduces the
-    eager step's outputs."""
+    """The step captured as a CUDA graph reproduces the eager step's outputs."""
     from two_level_sparse_gb300.step import IndexerStep
 
     wl = synth.config_workload(cid, device="cuda")

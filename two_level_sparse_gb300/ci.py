@@ -43,6 +43,8 @@ SIGNATURES = {
     "ci_prefill_tail": [_P, _I32, _P, _I32, _P, _I64, _P, _I32, _P, _P, _I64, _P, _P, _I32, _P, _P],
     "ci_select_sparse": [_P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _I32, _I32,
                          _I32, _P, _P, _I64, _P, _P],
+    "ci_select_sparse_layers": [_I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _P,
+                                _P, _P, _I32, _I32, _P, _P, _I64, _P, _P],
     "ci_dcp_merge_keys": [_P, _I32, _I64, _I64, _P, _I32, _I32, _I32, _P, _I64, _P, _P],
     "ci_dcp_merge_topk": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _I64, _P],
     "ci_q_rope_quant": [_P, _P, _P, _I32, _P, ctypes.c_float, ctypes.c_float, _I32, _I32, _I32, _P, _P, _P, _P, _P],
@@ -193,6 +195,46 @@ def ci_select_sparse(q_fp4, q_sf, w, k_pool, page_table, layout, seq_len, max_le
         rows, int(max_len), _ptr(blocks), int(blocks.stride(0)), _ptr(nvalid), int(max_blocks), int(block_positions),
         int(topk), _ptr(out_pos),
         _ptr(out_score), int(out_pos.stride(0)), _ptr(dev_err), _stream(stream)))
+
+
+def ci_select_sparse_layers(layers, page_table, layout, seq_len, max_len, topk, dev_err=None, stream=None,
+                            req_start=None, block_positions=8):
+    """Several layers' top-k positions in one launch (see include/ci.h).
+
+    ``layers``: a sequence of dicts with the per-layer tensors q_fp4, q_sf, w,
+    k_pool, blocks, nvalid, out_pos, the int max_blocks, and optionally
+    out_score; every k_pool has the same format and page count, every out_pos
+    the same row stride."""
+    n = len(layers)
+    if not 1 <= n <= 8:
+        raise ValueError("1 to 8 layers per launch")
+    for ly in layers:
+        for key, d in (("q_fp4", torch.uint8), ("q_sf", torch.uint8), ("w", torch.float32), ("k_pool", torch.uint8),
+                       ("blocks", torch.int32), ("nvalid", torch.int32), ("out_pos", torch.int32)):
+            _expect(ly[key], d, key)
+        if ly.get("out_score") is not None:
+            _expect(ly["out_score"], torch.float32, "out_score")
+    for t, d, name in ((page_table, torch.int32, "page_table"), (seq_len, torch.int32, "seq_len")):
+        _expect(t, d, name)
+    k0 = layers[0]["k_pool"]
+    if any(kv_format(ly["k_pool"]) != kv_format(k0) or ly["k_pool"].shape[0] != k0.shape[0] for ly in layers):
+        raise ValueError("every layer's pool needs the same page format and page count")
+    stride = int(layers[0]["out_pos"].stride(0))
+    if any(int(ly["out_pos"].stride(0)) != stride for ly in layers):
+        raise ValueError("every layer's out_pos needs the same row stride")
+
+    def arr(ctype, vals):
+        return (ctype * n)(*vals)
+
+    ptrs = lambda key: arr(_P, [_ptr(ly.get(key)) for ly in layers])  # noqa: E731
+    scores = ptrs("out_score") if any(ly.get("out_score") is not None for ly in layers) else None
+    rows = int(seq_len.shape[0])
+    _check("ci_select_sparse_layers", lib.ci_select_sparse_layers(
+        n, ptrs("q_fp4"), ptrs("q_sf"), ptrs("w"), ptrs("k_pool"), int(k0.shape[0]), kv_format(k0), _ptr(page_table),
+        int(page_table.shape[0]), int(page_table.shape[1]), int(layout), _req_start(layout, req_start), _ptr(seq_len),
+        rows, int(max_len), ptrs("blocks"), arr(_I64, [int(ly["blocks"].stride(0)) for ly in layers]), ptrs("nvalid"),
+        arr(_I32, [int(ly["max_blocks"]) for ly in layers]), int(block_positions), int(topk), ptrs("out_pos"), scores,
+        stride, _ptr(dev_err), _stream(stream)))
 
 
 def ci_q_rope_quant(positions, q, cos_sin, w, softmax_scale, head_scale, is_neox, out_format, q_out, q_sf, w_out,

@@ -97,7 +97,7 @@ int block_shift_of(int32_t block_positions) {
 
 extern "C" {
 
-int ci_version(void) { return 300; }
+int ci_version(void) { return 301; }
 
 const char* ci_strerror(int status) {
   switch (status) {
@@ -224,35 +224,53 @@ int ci_dcp_merge_topk(const int32_t* pos_local, const float* score_local, int32_
   return launched(ci::launch_dcp_merge_topk(a, static_cast<cudaStream_t>(stream)));
 }
 
+int ci_select_sparse_layers(int32_t num_layers, const uint8_t* const* q_fp4, const uint8_t* const* q_sf,
+                            const float* const* w, const uint8_t* const* k_pool, int64_t num_pages, int32_t kv_format,
+                            const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
+                            const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len,
+                            const int32_t* const* blocks, const int64_t* blocks_stride,
+                            const int32_t* const* nvalid, const int32_t* max_blocks, int32_t block_positions,
+                            int32_t topk, int32_t* const* out_pos, float* const* out_score, int64_t out_stride,
+                            int32_t* dev_err, void* stream) {
+  if (num_layers < 1 || num_layers > ci::kMaxSelectLayers) return CI_ERR_RANGE;
+  if (!q_fp4 || !q_sf || !w || !k_pool || !blocks || !blocks_stride || !nvalid || !max_blocks || !out_pos)
+    return CI_ERR_NULL;
+  ci::SelectArgs a{};
+  for (int l = 0; l < num_layers; ++l) {
+    int st = check_pool(q_fp4[l], q_sf[l], w[l], k_pool[l], num_pages, kv_format, page_table, num_req, max_pages,
+                        layout, req_row_start, seq_len, rows, max_len);
+    if (st != CI_OK) return st;
+    if (max_blocks[l] < 0 || max_blocks[l] > 2176) return CI_ERR_RANGE;
+    if (rows == 0) continue;
+    if (!blocks[l] || !nvalid[l] || !out_pos[l]) return CI_ERR_NULL;
+    if (blocks_stride[l] < max_blocks[l]) return CI_ERR_SHAPE;
+    a.layer[l] = ci::SelectLayer{q_fp4[l], q_sf[l], w[l], k_pool[l], blocks[l], blocks_stride[l], nvalid[l],
+                                 max_blocks[l], out_pos[l], out_score != nullptr ? out_score[l] : nullptr};
+  }
+  if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
+  const int shift = block_shift_of(block_positions);
+  if (shift < 0) return CI_ERR_RANGE;
+  if (num_pages > (int64_t{1} << 21)) return CI_ERR_RANGE;  // page ids are packed into 21 bits
+  if (rows == 0) return CI_OK;
+  if (out_stride < topk) return CI_ERR_SHAPE;
+  a.p = ci::PoolArgs{nullptr, nullptr, nullptr, nullptr, num_pages, kv_format, page_table, max_pages, layout,
+                     req_row_start, num_req, seq_len, rows, max_len, dev_err};
+  a.block_shift = shift;
+  a.topk = topk;
+  a.out_stride = out_stride;
+  a.num_layers = num_layers;
+  return launched(ci::launch_select(a, static_cast<cudaStream_t>(stream)));
+}
+
 int ci_select_sparse(const uint8_t* q_fp4, const uint8_t* q_sf, const float* w, const uint8_t* k_pool,
                      int64_t num_pages, int32_t kv_format, const int32_t* page_table, int32_t num_req, int32_t max_pages, int32_t layout,
                      const int32_t* req_row_start, const int32_t* seq_len, int32_t rows, int32_t max_len,
                      const int32_t* blocks, int64_t blocks_stride, const int32_t* nvalid, int32_t max_blocks,
                      int32_t block_positions, int32_t topk, int32_t* out_pos, float* out_score, int64_t out_stride,
                      int32_t* dev_err, void* stream) {
-  int st = check_pool(q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, num_req, max_pages, layout,
-                      req_row_start, seq_len, rows, max_len);
-  if (st != CI_OK) return st;
-  if (topk < 1 || topk > 2048) return CI_ERR_RANGE;
-  if (max_blocks < 0 || max_blocks > 2176) return CI_ERR_RANGE;
-  const int shift = block_shift_of(block_positions);
-  if (shift < 0) return CI_ERR_RANGE;
-  if (num_pages > (int64_t{1} << 21)) return CI_ERR_RANGE;  // page ids are packed into 21 bits
-  if (rows == 0) return CI_OK;
-  if (!blocks || !nvalid || !out_pos) return CI_ERR_NULL;
-  if (blocks_stride < max_blocks || out_stride < topk) return CI_ERR_SHAPE;
-  ci::SelectArgs a{{q_fp4, q_sf, w, k_pool, num_pages, kv_format, page_table, max_pages, layout, req_row_start, num_req, seq_len,
-                    rows, max_len, dev_err},
-                   shift,
-                   blocks,
-                   blocks_stride,
-                   nvalid,
-                   max_blocks,
-                   topk,
-                   out_pos,
-                   out_score,
-                   out_stride};
-  return launched(ci::launch_select(a, static_cast<cudaStream_t>(stream)));
+  return ci_select_sparse_layers(1, &q_fp4, &q_sf, &w, &k_pool, num_pages, kv_format, page_table, num_req, max_pages,
+                                 layout, req_row_start, seq_len, rows, max_len, &blocks, &blocks_stride, &nvalid,
+                                 &max_blocks, block_positions, topk, &out_pos, &out_score, out_stride, dev_err, stream);
 }
 
 }  // extern "C"

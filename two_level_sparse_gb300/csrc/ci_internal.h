@@ -51,17 +51,29 @@ struct PublishArgs {
   int32_t* dev_err;
 };
 
-struct SelectArgs {
-  PoolArgs p;
-  int32_t block_shift;  // log2 of the positions per candidate block: 3, or 2/1/0 for a context shard
+// One layer of a select launch: its query, weights, index-K pool, candidate
+// blocks and outputs.  The page table, layout and lengths are shared.
+constexpr int kMaxSelectLayers = 8;
+struct SelectLayer {
+  const uint8_t* q_fp4;
+  const uint8_t* q_sf;
+  const float* w;
+  const uint8_t* k_pool;
   const int32_t* blocks;
   int64_t blocks_stride;
   const int32_t* nvalid;
   int32_t max_blocks;
-  int32_t topk;
   int32_t* out_pos;
   float* out_score;
+};
+
+struct SelectArgs {
+  PoolArgs p;  // the shared page table, layout, lengths and pool format (its q / w / k_pool fields unused)
+  int32_t block_shift;  // log2 of the positions per candidate block: 3, or 2/1/0 for a context shard
+  int32_t topk;
   int64_t out_stride;
+  int32_t num_layers;  // 1 .. kMaxSelectLayers; work units are (layer, row), layer-major
+  SelectLayer layer[kMaxSelectLayers];
 };
 
 // Each returns a cudaError_t from the launch (cudaSuccess when enqueued).

@@ -10,7 +10,11 @@
 // blocks read from the paged index-K pool, top-512 of the first valid_len
 // columns, page transform to request-relative positions).
 //
-// One persistent CTA per SM works through its rows; consecutive rows overlap:
+// One launch scores up to eight layers that share a page table (the source
+// with its own top-(P+1) blocks, the consumers with the published ones): the
+// work units are (layer, row) pairs, layer-major, so that one layer's pool is
+// live in L2 at a time.  One persistent CTA per SM works through its units;
+// consecutive units overlap (a unit is called a row below):
 //   warp 0      MMA issuer: per row, tcgen05.cp of the row's query scale
 //               factors into tensor memory, then per 128-position tile four
 //               tcgen05.mma kind::mxf8f6f4 block_scale (M = 128 gathered
@@ -124,20 +128,39 @@ __device__ __forceinline__ int row_request(const SelectArgs& a, int row) {
 }
 
 struct RowInfo {
-  int row, L, nv, nb, ntiles;
+  int layer, row, L, nv, nb, ntiles;
 };
 
-__device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int row, bool report_errors) {
+// kMulti: the launch scores several layers and a unit's per-layer pointers
+// come from a dynamically indexed kernel parameter; pinned in a register once
+// per unit, they are not re-read from the constant bank at every use inside
+// the tile loops.  A one-layer launch (kMulti false) reads layer 0's fields
+// as constant-bank operands, as a fixed parameter.
+template <bool kMulti, class T>
+__device__ __forceinline__ void pin(T*& p) {
+  if (kMulti) asm volatile("" : "+l"(p));
+}
+template <bool kMulti>
+__device__ __forceinline__ const SelectLayer& layer_of(const SelectArgs& a, int l) {
+  return a.layer[kMulti ? l : 0];
+}
+
+// Work unit u: layer u / rows, row u % rows.
+template <bool kMulti>
+__device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int u, bool report_errors) {
   RowInfo r;
-  r.row = row;
+  r.layer = kMulti ? u / a.p.rows : 0;
+  r.row = kMulti ? u - r.layer * a.p.rows : u;
+  const int row = r.row;
+  const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
   r.L = a.p.seq_len[row];
-  r.nv = a.nvalid[row];
+  r.nv = ly.nvalid[row];
   bool bad = false;
   if (r.L < 0 || r.L > a.p.max_len) {
     if (report_errors) report(a.p.dev_err, kDevErrLen);
     bad = true;
   }
-  if (r.nv < 0 || r.nv > a.max_blocks) {
+  if (r.nv < 0 || r.nv > ly.max_blocks) {
     if (report_errors) report(a.p.dev_err, kDevErrBlock);
     bad = true;
   }
@@ -162,18 +185,25 @@ struct Ring {
 // swizzled B tile, its scale factors staged for tcgen05.cp, and for every
 // candidate block its physical page, its slot in the page and how many of its
 // positions lie below L.
-template <int KV>
+template <int KV, bool kMulti>
 __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
                                          volatile int* abort_flag) {
   const int b = ri & 1;
   const uint32_t ph = (ri >> 1) & 1;
+  const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
+  const uint8_t* q_fp4 = ly.q_fp4 + static_cast<int64_t>(r.row) * kHeads * 64;
+  const uint8_t* q_sf = ly.q_sf + static_cast<int64_t>(r.row) * kHeads * 4;
+  const int32_t* brow = ly.blocks + static_cast<int64_t>(r.row) * ly.blocks_stride;
+  pin<kMulti>(q_fp4);
+  pin<kMulti>(q_sf);
+  pin<kMulti>(brow);
   bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
   if (KV == kKvMxfp4) {
     // packed e2m1 rows of 64 bytes, 64-byte swizzle
     for (int idx = pid_t; ok && idx < kHeads * 4; idx += kPrepThreads) {
       const int head = idx >> 2, c = idx & 3;
       const uint2* src =
-          reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(r.row) * kHeads + head) * 64 + c * 16);
+          reinterpret_cast<const uint2*>(q_fp4 + head * 64 + c * 16);
       const uint2 lo = src[0], hi = src[1];
       *reinterpret_cast<uint4*>(sm.q[b] + sw64_offset(head, c * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
@@ -181,13 +211,13 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
     for (int idx = pid_t; ok && idx < kHeads * 8; idx += kPrepThreads) {
       const int head = idx >> 3, c = idx & 7;
       const uint2 packed =
-          *reinterpret_cast<const uint2*>(a.p.q_fp4 + (static_cast<int64_t>(r.row) * kHeads + head) * 64 + c * 8);
+          *reinterpret_cast<const uint2*>(q_fp4 + head * 64 + c * 8);
       *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(head, c * 16)) = widen_fp4x16(packed);
     }
   }
   if (ok && pid_t < 32) {
     // lane l of the scale-factor columns: heads l and 32 + l, byte j = K block j
-    const uint32_t* sfp = reinterpret_cast<const uint32_t*>(a.p.q_sf + static_cast<int64_t>(r.row) * kHeads * 4);
+    const uint32_t* sfp = reinterpret_cast<const uint32_t*>(q_sf);
     *reinterpret_cast<uint4*>(sm.sf[b] + 16 * pid_t) =
         make_uint4(sfp[pid_t], sfp[32 + pid_t], kUnitScales, kUnitScales);
   }
@@ -196,7 +226,6 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
   ok = ok && warp_wait(&sm.info_empty[b], ph ^ 1, abort_flag);  // row ri - 2 gathered and scored
   const int req = row_request(a, r.row);
   const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
-  const int32_t* brow = a.blocks + static_cast<int64_t>(r.row) * a.blocks_stride;
   constexpr int kBatch = 16;
   for (int i0 = 0; ok && i0 < r.nv; i0 += kPrepThreads * kBatch) {
     int blk[kBatch], pid[kBatch];
@@ -468,9 +497,14 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   }
 }
 
-template <int KV>
+// The layers' tensor maps over their pools (8-row boxes).
+struct SelectMaps {
+  CUtensorMap m[kMaxSelectLayers];
+};
+
+template <int KV, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1)
-    select_kernel(const __grid_constant__ CUtensorMap tmap, const SelectArgs a) {
+    select_kernel(const __grid_constant__ SelectMaps maps, const SelectArgs a) {
   constexpr bool kFp4 = KV == kKvMxfp4;
   constexpr int kBlockBytes = kBlock * row_bytes<KV>();  // one candidate block's values: 1 KB or 512 B
   constexpr int kPVB = page_value_bytes<KV>(), kPB = page_bytes<KV>();
@@ -506,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmap);
+    for (int l = 0; l < a.num_layers; ++l) prefetch_tmap(&maps.m[l]);
   }
   tc_fence_before();
   __syncthreads();
@@ -521,14 +555,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  const int rows = a.p.rows;
+  const int rows = a.num_layers * a.p.rows;  // work units
   if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
     Ring kr, ar;
     int ri = 0;
     bool ok = true;
-    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
-      const RowInfo r = row_info(a, row, lane == 0);
+    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+      const RowInfo r = row_info<kMulti>(a, u, lane == 0);
       const int b = ri & 1;
       if (!warp_wait_fast(&sm.q_full[b], (ri >> 1) & 1, abort_flag)) {
         ok = false;
@@ -591,9 +625,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ri = 0;
     uint32_t issued = 0;  // warp 1: tiles whose tensor-map loads were issued
     bool ok = true;
-    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
-      const RowInfo r = row_info(a, row, false);
+    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+      const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
+      const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
+      const CUtensorMap* tmap = &maps.m[kMulti ? r.layer : 0];
+      pin<kMulti>(k_pool);
+      pin<kMulti>(tmap);
       ok = warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t) {
@@ -612,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int blk = 0; blk < kTmaBlocks; ++blk) {
             const int vb = __shfl_sync(0xffffffffu, v, blk);
             if (vb >= 0)
-              tma_load_3d_elect(dst + blk * kBlockBytes, &tmap, 0, ((vb >> 7) & 7) * kBlock, vb >> 10,
+              tma_load_3d_elect(dst + blk * kBlockBytes, tmap, 0, ((vb >> 7) & 7) * kBlock, vb >> 10,
                                 &sm.tk_full[kr.idx]);
           }
           ++issued;
@@ -626,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int v = slot < r.nv ? info[slot] : -1;
             if (v >= 0) {
               const uint8_t* src =
-                  a.p.k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
+                  k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
               if (kFp4) {
                 cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
               } else {
@@ -645,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int v = slot < r.nv ? info[slot] : -1;
               if (v >= 0)
                 cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
-                          a.p.k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
+                          k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
             }
           }
           cp_async_arrive_noinc(&sm.k_full[kr.idx]);
@@ -669,8 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // prep of row index pi (the pi-th row of this CTA); the verdict is made uniform
     // across the four warps before anyone acts on it
     auto prep = [&](int pi) -> bool {
-      const int prow = blockIdx.x + pi * gridDim.x;
-      const bool mine = prow >= rows || prep_row<KV>(sm, a, row_info(a, prow, false), pi, kt, abort_flag);
+      const int pu = blockIdx.x + pi * gridDim.x;
+      const bool mine = pu >= rows || prep_row<KV, kMulti>(sm, a, row_info<kMulti>(a, pu, false), pi, kt, abort_flag);
       if (lane == 0) sm.prep_ok[warp & 3] = mine ? 1 : 0;
       named_sync(kTopkBar, kTopkThreads);
       const bool all = sm.prep_ok[0] && sm.prep_ok[1] && sm.prep_ok[2] && sm.prep_ok[3];
@@ -679,8 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = prep(0) && prep(1);
     int ri = 0;
-    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
-      const RowInfo r = row_info(a, row, false);
+    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+      const RowInfo r = row_info<kMulti>(a, u, false);
+      const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
       const int b = ri & 1;
       if (kt == 0) sm.topk_go = mbar_wait(&sm.sc_full[b], (ri >> 1) & 1, abort_flag) ? 1 : 0;
       named_sync(kTopkBar, kTopkThreads);
@@ -690,8 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int k = min(a.topk, sm.vcount[b]);
-      int32_t* out = a.out_pos + static_cast<int64_t>(row) * a.out_stride;
-      float* osc = a.out_score != nullptr ? a.out_score + static_cast<int64_t>(row) * a.out_stride : nullptr;
+      int32_t* out = ly.out_pos + static_cast<int64_t>(r.row) * a.out_stride;
+      float* osc = ly.out_score != nullptr ? ly.out_score + static_cast<int64_t>(r.row) * a.out_stride : nullptr;
+      pin<kMulti>(out);
+      pin<kMulti>(osc);
       if (k > 0) {
         tmem_topk(
             sm, lane_base + kScoreCol + b * kMaxTiles, r.ntiles, k, kt,
@@ -724,10 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ri = 0;
     unsigned long long w2[32];  // head weights, packed pairs
     bool ok = true;
-    for (int row = blockIdx.x; row < rows && ok; row += gridDim.x, ++ri) {
-      const RowInfo r = row_info(a, row, false);
+    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+      const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
-      load_head_weights(w2, a.p.w + static_cast<int64_t>(row) * kHeads);
+      const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
+      pin<kMulti>(k_pool);
+      load_head_weights(w2, layer_of<kMulti>(a, r.layer).w + static_cast<int64_t>(r.row) * kHeads);
       // the candidate page lookups (prepared with the row) tell which positions are live
       if (!warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag) ||
           (ri >= 2 && !warp_wait(&sm.sc_empty[b], ((ri >> 1) & 1) ^ 1, abort_flag))) {
@@ -747,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // (MXFP4: 1, the scales are inside the MMA)
           float kscale = kFp4 ? 1.0f : 0.0f;
           if (!kFp4 && valid)
-            kscale = __ldg(reinterpret_cast<const float*>(a.p.k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB) +
+            kscale = __ldg(reinterpret_cast<const float*>(k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB) +
                            ((v >> 7) & 7) * kBlock + (p & 7));
           if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
             ok = false;
@@ -802,22 +845,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t select_smem_bytes(int) { return sizeof(Smem) + 1024; }
 
-template <int KV>
+template <int KV, bool kMulti>
 cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
-  const int smem = static_cast<int>(select_smem_bytes(a.max_blocks));
-  cudaError_t e = cudaFuncSetAttribute(select_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = static_cast<int>(select_smem_bytes(0));
+  cudaError_t e = cudaFuncSetAttribute(select_kernel<KV, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  CUtensorMap tmap;
-  e = make_pool_tmap(&tmap, a.p.k_pool, a.p.num_pages, KV, kBlock);
-  if (e != cudaSuccess) return e;
-  const int grid = min(device_sm_count(), a.p.rows);
-  select_kernel<KV><<<grid, kThreads, smem, stream>>>(tmap, a);
+  SelectMaps maps;
+  for (int l = 0; l < a.num_layers; ++l) {
+    e = make_pool_tmap(&maps.m[l], a.layer[l].k_pool, a.p.num_pages, KV, kBlock);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t units = static_cast<int64_t>(a.num_layers) * a.p.rows;
+  const int grid = units < device_sm_count() ? static_cast<int>(units) : device_sm_count();
+  select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
-  if (a.p.rows == 0) return cudaSuccess;
-  return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4>(a, stream) : launch_select_kv<kKvFp8>(a, stream);
+  if (a.p.rows == 0 || a.num_layers == 0) return cudaSuccess;
+  if (a.num_layers > 1)
+    return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, true>(a, stream)
+                                     : launch_select_kv<kKvFp8, true>(a, stream);
+  return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, false>(a, stream)
+                                   : launch_select_kv<kKvFp8, false>(a, stream);
 }
 
 }  // namespace ci
