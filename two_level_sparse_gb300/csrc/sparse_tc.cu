@@ -144,6 +144,16 @@ template <bool kMulti>
 __device__ __forceinline__ const SelectLayer& layer_of(const SelectArgs& a, int l) {
   return a.layer[kMulti ? l : 0];
 }
+// The i-th unit of this CTA.  One layer: round robin.  Several layers (their
+// order set by the launcher, the largest candidate lists first): a snake,
+// CTA c taking units c, 2G - 1 - c, 2G + c, ... of a grid of G, so that the
+// CTAs that took the last of the large units in one pass take the first of
+// the next pass's (smaller) ones.  Increasing in i for every CTA.
+template <bool kMulti>
+__device__ __forceinline__ int unit_of(int i) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return i * g + (kMulti && (i & 1) ? g - 1 - c : c);
+}
 
 // Work unit u: layer u / rows, row u % rows.
 template <bool kMulti>
@@ -561,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring kr, ar;
     int ri = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+    for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, lane == 0);
       const int b = ri & 1;
       if (!warp_wait_fast(&sm.q_full[b], (ri >> 1) & 1, abort_flag)) {
@@ -625,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ri = 0;
     uint32_t issued = 0;  // warp 1: tiles whose tensor-map loads were issued
     bool ok = true;
-    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+    for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
       const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
@@ -707,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // prep of row index pi (the pi-th row of this CTA); the verdict is made uniform
     // across the four warps before anyone acts on it
     auto prep = [&](int pi) -> bool {
-      const int pu = blockIdx.x + pi * gridDim.x;
+      const int pu = unit_of<kMulti>(pi);
       const bool mine = pu >= rows || prep_row<KV, kMulti>(sm, a, row_info<kMulti>(a, pu, false), pi, kt, abort_flag);
       if (lane == 0) sm.prep_ok[warp & 3] = mine ? 1 : 0;
       named_sync(kTopkBar, kTopkThreads);
@@ -717,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = prep(0) && prep(1);
     int ri = 0;
-    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+    for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, false);
       const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
       const int b = ri & 1;
@@ -765,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ri = 0;
     unsigned long long w2[32];  // head weights, packed pairs
     bool ok = true;
-    for (int u = blockIdx.x; u < rows && ok; u += gridDim.x, ++ri) {
+    for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
       const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
@@ -863,9 +873,18 @@ cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   if (a.p.rows == 0 || a.num_layers == 0) return cudaSuccess;
-  if (a.num_layers > 1)
-    return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, true>(a, stream)
-                                     : launch_select_kv<kKvFp8, true>(a, stream);
+  if (a.num_layers > 1) {
+    // layers with the most candidate blocks first (stable), for the snake order
+    SelectArgs s = a;
+    for (int i = 1; i < s.num_layers; ++i)
+      for (int j = i; j > 0 && s.layer[j].max_blocks > s.layer[j - 1].max_blocks; --j) {
+        const SelectLayer t = s.layer[j];
+        s.layer[j] = s.layer[j - 1];
+        s.layer[j - 1] = t;
+      }
+    return s.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, true>(s, stream)
+                                     : launch_select_kv<kKvFp8, true>(s, stream);
+  }
   return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, false>(a, stream)
                                    : launch_select_kv<kKvFp8, false>(a, stream);
 }
