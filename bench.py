@@ -556,8 +556,10 @@ def main():
             r = measure(cid, max(3, args.steps // 2), 3, stream, flush)
             mst = statistics.mean(r["t_step"])
             msd = statistics.mean(r["t_dense"])
+            mss = statistics.mean(r["t_select"])
             msg = graph_step_ms(r["step"], max(3, args.steps // 2), stream, flush)
             f, b, _ = algorithmic_counts(r["wl"])
+            sb = select_bytes(r["wl"])
             rows = r["wl"].rows
             secondary.append({
                 "metric": "decode rows/s", "workload": r["wl"].name, "value": world * rows / (mst * 1e-3),
@@ -566,6 +568,11 @@ def main():
                           "note": "the same step replayed as a CUDA graph"},
                 "dense_roofline": {"bound": "hbm", "achieved": b / (msd * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                                    "unit": "GB/s", "frac": b / (msd * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                "select_roofline": {"bound": "hbm", "achieved": sb / (mss * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                                    "unit": "GB/s", "frac": sb / (mss * 1e-3) / 1e9 / peaks["hbm_gbs"], "ms": mss,
+                                    "launches": r["launches"] - 2,
+                                    "note": "candidate K gathered by the five layers' selects (pools larger than L2: "
+                                            "from HBM) / select time"},
                 "dev_err": int(r["step"].dev_err.item()),
             })
             del r
