@@ -17,7 +17,9 @@
 // bins.  That histogram serves both selections; two 10-bit passes over the
 // keys sharing the chosen prefix finish each threshold (skipped as soon as
 // the threshold bucket is taken whole).  An ordered compaction per selection
-// writes the winners in ascending id order, so no sort is needed.
+// writes the winners in ascending id order, so no sort is needed; the
+// narrower selection compacts only the wider one's winners (its top K' lie
+// inside the top K >= K' under the same order).
 #include "ci_common.cuh"
 #include "ci_internal.h"
 
@@ -81,14 +83,17 @@ __device__ __forceinline__ void find_digit(const uint32_t* hist, int nbins, cons
 
 // Ordered compaction of the keys above the threshold (prefix under mask) and
 // the first need_eq at it, in index order: warps own contiguous segments.
+// Candidates are the block ids 0 .. n - 1, or, with ids, the n ascending ids
+// ids[0 .. n - 1] (a wider selection's winners).
 __device__ __forceinline__ void emit_selected(const uint32_t* sk, int n, uint32_t prefix, uint32_t mask,
-                                              uint32_t need_eq, int32_t* out, PublishShared& sh, int tid) {
+                                              uint32_t need_eq, int32_t* out, PublishShared& sh, int tid,
+                                              const int32_t* ids = nullptr) {
   const int wid = tid >> 5, lane = tid & 31;
   const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
   const int begin = min(n, wid * seg), end = min(n, begin + seg);
   uint32_t gt = 0, eq = 0;
   for (int i = begin + lane; i < end; i += 32) {
-    const uint32_t m = sk[i] & mask;
+    const uint32_t m = sk[ids != nullptr ? ids[i] : i] & mask;
     gt += m > prefix;
     eq += m == prefix;
   }
@@ -108,13 +113,14 @@ __device__ __forceinline__ void emit_selected(const uint32_t* sk, int n, uint32_
   for (int base = begin; base < end; base += 32) {
     const int i = base + lane;
     const bool valid = i < end;
-    const uint32_t m = valid ? sk[i] & mask : 0u;
+    const int id = valid ? (ids != nullptr ? ids[i] : i) : 0;
+    const uint32_t m = valid ? sk[id] & mask : 0u;
     const bool is_gt = valid && m > prefix;
     const bool is_eq = valid && m == prefix;
     const uint32_t bg = __ballot_sync(0xffffffffu, is_gt);
     const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
     const uint32_t eq_rank = eq_before + __popc(be & lt);
-    if (is_gt || (is_eq && eq_rank < need_eq)) out[gt_before + __popc(bg & lt) + min(eq_rank, need_eq)] = i;
+    if (is_gt || (is_eq && eq_rank < need_eq)) out[gt_before + __popc(bg & lt) + min(eq_rank, need_eq)] = id;
     gt_before += __popc(bg);
     eq_before += __popc(be);
   }
@@ -211,9 +217,16 @@ __global__ void __launch_bounds__(kThreads, 1) publish_kernel(const PublishArgs 
       open[s] = sh.match[s] != sh.rem[s];
     }
   }
-#pragma unroll
-  for (int s = 0; s < 2; ++s)
-    if (want[s]) emit_selected(sk, nb, prefix[s], mask[s], need[s], out[s], sh, tid);
+  if (want[0]) emit_selected(sk, nb, prefix[0], mask[0], need[0], out[0], sh, tid);
+  if (want[1]) {
+    // The top K' (ties toward the lower id) lie inside the top K >= K': pick
+    // them from the first selection's K ascending winners (visible to the
+    // whole CTA after emit_selected's closing barrier) instead of all keys.
+    if (want[0] && want[1] <= want[0])
+      emit_selected(sk, static_cast<int>(want[0]), prefix[1], mask[1], need[1], out[1], sh, tid, out[0]);
+    else
+      emit_selected(sk, nb, prefix[1], mask[1], need[1], out[1], sh, tid);
+  }
 }
 
 }  // namespace
