@@ -209,6 +209,13 @@ def test_select_layers_host_checks(ci):
     assert f(*bad) == -2
 
 
+def test_select_layers_binding_checks_the_layer_count(ci):
+    with pytest.raises(ValueError):
+        ci.ci_select_sparse_layers([], None, 0, None, 0, 8)
+    with pytest.raises(ValueError):
+        ci.ci_select_sparse_layers([{}] * 9, None, 0, None, 0, 8)
+
+
 def test_dcp_merge_host_checks(ci):
     fk, ft = ci.lib.ci_dcp_merge_keys, ci.lib.ci_dcp_merge_topk
     assert fk(P, 3, 64, 8, P, 4, 64, 0, P, 8, N, N) == -4   # world not 2, 4 or 8
