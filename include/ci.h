@@ -140,7 +140,11 @@ enum ci_q_format { CI_Q_MXFP4 = 0, CI_Q_FP8 = 1 };
  * with logit[t, s] = kscale[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s]) computed in
  * fp32 (products exact, fp32 accumulation; kscale = 1 for CI_KV_MXFP4, whose
  * scales are part of k), and keys[t*keys_stride + nb_t - 1]
- * = +inf.  Rows with nb_t <= skip_le_blocks are not scored and their keys are
+ * = +inf.  Precondition: every FP8 position scale kscale[s] is finite and
+ * positive.  The method's score is sum_h w * ReLU(q . (kscale * k)); only for
+ * kscale > 0 may the scale leave the ReLU, so for a zero, negative or
+ * non-finite scale the result is this formula, not the method's score (the
+ * kernels do not check it).  Rows with nb_t <= skip_le_blocks are not scored and their keys are
  * left untouched (sglang PR #40352, Design, "Level one"; the block_amax.cuh
  * listing in the same PR's review: max of 8, last key +inf, rows with at most
  * topk blocks skipped).  The [rows, L] score matrix is never written.
@@ -191,7 +195,11 @@ CI_API int ci_publish_blocks(const int32_t* seq_len, int32_t rows, int32_t max_l
  * top P + 1 (sglang PR #40352, Design, "Level one").  blocks2 == NULL makes it
  * ci_publish_blocks (topk_blocks2, blocks2_stride and nvalid2 are then
  * ignored); otherwise nvalid2 must not be NULL, 1 <= topk_blocks2 <= 16384 and
- * blocks2_stride >= topk_blocks2.  Same errors as ci_publish_blocks.
+ * blocks2_stride >= topk_blocks2.  The two tables must not overlap: the
+ * narrower selection is read back from the wider one's table while it is
+ * written, so the int32 ranges [blocks, blocks + (rows - 1) * blocks_stride +
+ * topk_blocks) and the same for blocks2 must be disjoint (CI_ERR_SHAPE
+ * otherwise).  Same errors as ci_publish_blocks.
  */
 CI_API int ci_publish_blocks2(const int32_t* seq_len, int32_t rows, int32_t max_len, const float* keys,
                        int64_t keys_stride, int32_t topk_blocks, int32_t* blocks, int64_t blocks_stride,

@@ -31,9 +31,9 @@ What it computes follows these passages:
 * the source layer's own top-512 is the plain dense top-512 over all
   ``s < L_t`` (PR #40352, Design: the source "runs its own top-512").
 
-Readings where the pages are silent (each also listed in the design doc): ties are
-broken toward the lower index, for blocks and for positions; element ``2i`` of
-an MXFP4 byte pair is the low nibble.
+Readings where the pages are silent: ties are broken toward the lower index,
+for blocks and for positions; element ``2i`` of an MXFP4 byte pair is the low
+nibble.
 """
 from __future__ import annotations
 

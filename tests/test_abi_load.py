@@ -101,6 +101,12 @@ def test_publish_pair_host_checks(ci):
     assert f(P, 2, 64, P, 8, 16, P, 16, P, 20, P, 16, P, N, N) == -2  # blocks2 stride < topk_blocks2
     assert f(P, 2, 64, P, 8, 16, P, 16, P, 4, P, 4, N, N, N) == -1  # nvalid2 missing
     assert f(P, 2, 64, P, 8, 0, P, 16, P, 4, N, 4, N, N, N) == -4  # first selection checked as before
+    # the two tables may not share a byte (the second is read back from the first while it is written)
+    assert f(P, 2, 64, P, 8, 16, P, 16, P, 4, P, 4, P, N, N) == -2  # the same table twice
+    inside = ctypes.c_void_p(0x1000 + 4 * 20)  # row 1 of a [2][16] table
+    assert f(P, 2, 64, P, 8, 16, P, 16, P, 4, inside, 4, P, N, N) == -2
+    below = ctypes.c_void_p(0x1000 - 4 * 10)  # a [2][4] table whose last row runs into the first table
+    assert f(P, 2, 64, P, 8, 16, P, 16, P, 4, below, 8, P, N, N) == -2
 
 
 def test_prefill_tail_host_checks(ci):

@@ -555,8 +555,10 @@ def test_q_producer_feeds_the_indexer(ci):
 @pytest.mark.parametrize("case", ["decode", "prefill", "varlen"])
 def test_dcp_step_equals_unsharded_step_bitwise(ci, world, case):
     """W context shards (interleave 1): local block maxima merged across shards,
-    local top-512 merged across shards -- the same keys, blocks, positions and
-    scores as the unsharded step, bit for bit."""
+    local top-512 merged across shards -- the oracle's keys, blocks, positions
+    and scores (vLLM sparse_attn_indexer.py: the MAX-reduce of block scores
+    with the global newest block pinned, and _merge_dcp_topk_global's exact
+    merge), and bit for bit the unsharded step's."""
     from two_level_sparse_gb300.dcp import DcpStep
     from two_level_sparse_gb300.step import IndexerStep
 
@@ -574,12 +576,33 @@ def test_dcp_step_equals_unsharded_step_bitwise(ci, world, case):
     torch.cuda.synchronize()
     assert int(d.dev_err.item()) == 0 and int(ref.dev_err.item()) == 0
     a, b = ref.outputs_numpy(), d.outputs_numpy()
+    assert_ok(compare.check_step(wl, b))
     for k in ("blocks", "nvalid", "blocks_src", "nvalid_src", "pos"):
         np.testing.assert_array_equal(b[k], a[k], err_msg=k)
     np.testing.assert_array_equal(b["score"].view(np.uint32), a["score"].view(np.uint32))
     nb = (wl.seq_len.numpy() + 7) // 8
     for t in np.nonzero(nb > min(wl.topk_blocks, wl.topk + 1))[0]:
         np.testing.assert_array_equal(b["keys"][t, : nb[t]].view(np.uint32), a["keys"][t, : nb[t]].view(np.uint32))
+
+
+@needs_cuda
+def test_dcp_full_size_prefill_chunk_sampled_rows(ci):
+    """The 16384-row chunk at 262144 positions as 2 context shards: the merged
+    keys, published blocks and every layer's top-512 of sampled rows against
+    the oracle (the exact merge of vLLM sparse_attn_indexer.py,
+    _merge_dcp_topk_global)."""
+    from two_level_sparse_gb300.dcp import DcpStep
+
+    wl_dev = synth.config_workload(4, device="cuda")
+    d = DcpStep(wl_dev, 2)
+    d.run()
+    torch.cuda.synchronize()
+    assert int(d.dev_err.item()) == 0
+    rows = [0, 8191, 16383]
+    out = d.outputs_numpy()
+    sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
+    del d
+    assert_ok(compare.check_step(subset_workload(wl_dev, rows), sub_out))
 
 
 @needs_cuda

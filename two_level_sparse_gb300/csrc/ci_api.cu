@@ -151,6 +151,14 @@ int ci_publish_blocks2(const int32_t* seq_len, int32_t rows, int32_t max_len, co
   if (blocks2 != nullptr && !nvalid2) return CI_ERR_NULL;
   if (blocks_stride < topk_blocks) return CI_ERR_SHAPE;
   if (blocks2 != nullptr && blocks2_stride < topk_blocks2) return CI_ERR_SHAPE;
+  if (blocks2 != nullptr) {
+    // the K' selection reads the K selection's winners back while it writes:
+    // the two tables must not share a byte
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(blocks), b0 = reinterpret_cast<uintptr_t>(blocks2);
+    const uintptr_t a1 = a0 + (static_cast<uint64_t>(rows - 1) * blocks_stride + topk_blocks) * sizeof(int32_t);
+    const uintptr_t b1 = b0 + (static_cast<uint64_t>(rows - 1) * blocks2_stride + topk_blocks2) * sizeof(int32_t);
+    if (a0 < b1 && b0 < a1) return CI_ERR_SHAPE;
+  }
   if (keys_stride % 8 != 0 || keys_stride < (static_cast<int64_t>(max_len) + 7) / 8) return CI_ERR_SHAPE;
   if (!aligned(keys, 16)) return CI_ERR_ALIGN;
   ci::PublishArgs a{seq_len, rows,   max_len, keys, keys_stride, topk_blocks,
