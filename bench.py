@@ -26,6 +26,10 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+# The CPU oracle baseline runs one row per host thread; each numpy BLAS call
+# stays on its own thread (set before numpy is first imported, by torch).
+for _v in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
 
 import torch  # noqa: E402
 
@@ -66,6 +70,23 @@ def load_peaks():
             p = json.load(f)
         return p, "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# tcgen05 kind::mxf8f6f4 rate measured by this library's own microbenchmark
+# (M = 128, N >= 128, 152 SMs at 2070 MHz): context beside the derived peak.
+MXF8F6F4_PROBE_TFLOPS = 4860.0
+
+
+def tensor_peaks(peaks, src):
+    """Block-scaled tensor peaks derived from the measured dense bf16 burst
+    rate by the nominal ratios (bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s): FP8 x 2
+    for kind::mxf8f6f4 (MXFP4 queries against FP8 index-K), FP4 x 6 for
+    kind::mxf4 (MXFP4 against MXFP4)."""
+    bf16 = peaks["bf16_tflops"]
+    return {
+        "fp8": (2.0 * bf16, f"{src} bf16_tflops (burst) x 2, the fp8 / bf16 nominal ratio (kind::mxf8f6f4)"),
+        "fp4": (6.0 * bf16, f"{src} bf16_tflops (burst) x 6, the fp4 / bf16 nominal ratio (kind::mxf4)"),
+    }
 
 
 class ClockSampler:
@@ -146,16 +167,16 @@ def k_position_bytes(wl):
     return 68 if wl.kv == 1 else 132
 
 
-def select_bytes(wl):
-    """Algorithmic bytes of the step's five sparse-scorer launches.
+def select_work(wl):
+    """Algorithmic work of the step's sparse-scorer launches (the source with
+    its K' = P + 1 blocks, every consumer with K).
 
-    Per candidate position 132 bytes (128 e4m3 + one fp32 scale; 68 for MXFP4
-    pools) gathered; per
-    row and launch the query, its scales and weights (4608 bytes), the block
-    ids (4 per block) and the output positions (4 per pick).  A row with
-    nb_t <= K' blocks scores all L_t positions; otherwise K' - 1 full blocks
-    plus its newest (partial) block.  The source runs with K' = P + 1 blocks,
-    each consumer with K.
+    Returns ``(positions, gathered, other)``: candidate positions scored (each
+    2 * 64 * 128 flops), index-K bytes gathered for them (132 per position:
+    128 e4m3 + one fp32 scale; 68 for MXFP4 pools), and the per-row bytes
+    (query, scales and weights 4608, block ids 4 per block, output positions
+    4 per pick).  A row with nb_t <= K' blocks scores all L_t positions;
+    otherwise K' - 1 full blocks plus its newest (partial) block.
     """
     L = wl.seq_len.to(torch.int64).cpu()
     nb = (L + 7) // 8
@@ -165,9 +186,20 @@ def select_bytes(wl):
         full = nb > kb
         pos = torch.where(full, 8 * (kb - 1) + (L - 8 * (nb - 1)), L)
         blocks = torch.where(full, torch.full_like(nb, kb), nb)
-        return int((k_position_bytes(wl) * pos + 4608 + 4 * blocks + 4 * P).sum())
+        return int(pos.sum()), int((4608 + 4 * blocks + 4 * P).sum())
 
-    return one(P + 1) + (len(wl.layers) - 1) * one(K)
+    pos0, oth0 = one(P + 1)
+    posk, othk = one(K)
+    n = len(wl.layers) - 1
+    positions = pos0 + n * posk
+    return positions, k_position_bytes(wl) * positions, oth0 + n * othk
+
+
+def select_bytes(wl):
+    """Algorithmic bytes of the step's sparse-scorer launches (gathered K plus
+    the per-row bytes, see select_work)."""
+    _, gathered, other = select_work(wl)
+    return gathered + other
 
 
 def time_steps(step, steps, warmup, flush, stream, dense_events=True):
@@ -240,66 +272,106 @@ def e2e_time(step, steps, stream):
     return times[1:], h2d, d2h
 
 
-def cpu_oracle_sample(cid, budget_s=20.0):
-    """The oracle as it stands, on the host cores, over a bounded row sample of
-    workload `cid`; returns (ms per step extrapolated, rows timed, threads)."""
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sample_rows(n, cap=128):
+    """All rows when there are at most ``cap``; otherwise the first cap/4, the
+    last cap/4 and cap/2 evenly spaced rows between them."""
+    if n <= cap:
+        return list(range(n))
+    q = cap // 4
+    mid = [q + round(i * (n - 2 * q - 1) / (cap - 2 * q - 1)) for i in range(cap - 2 * q)]
+    return sorted(set(list(range(q)) + mid + list(range(n - q, n))))
+
+
+def oracle_rows_s(wl, rows, threads):
+    """Wall seconds of the oracle as it stands over ``rows`` of workload
+    ``wl`` (any device: the rows' operands and the pools are copied to the
+    host first, outside the timing), one row per host thread: the source
+    layer's dense scores, keys, published blocks and own top-P, then every
+    consumer's top-P within the published blocks."""
+    import concurrent.futures
+
     import numpy as np
 
     from oracle import ci_oracle as O
     from two_level_sparse_gb300 import synth
 
-    lens = synth.config_lengths(cid)
-    rows = [int(lens.shape[0]) - 1, 0, int(lens.shape[0]) // 2]
-    # operands of the sampled rows only (the whole pool comes along)
-    wl = synth.config_workload(cid, device="cuda" if torch.cuda.is_available() else "cpu")
-    pt = wl.page_table.cpu().numpy()
-    layers = [synth.Layer(l.q_fp4[rows].cpu(), l.q_sf[rows].cpu(), l.w[rows].cpu(), l.k_pool.cpu()) for l in wl.layers]
-    pts = pt[rows] if wl.layout == 0 else pt
+    idx = torch.tensor(rows, dtype=torch.long, device=wl.seq_len.device)
+    layers = [synth.Layer(l.q_fp4[idx].cpu(), l.q_sf[idx].cpu(), l.w[idx].cpu(), l.k_pool.cpu()) for l in wl.layers]
+    pt = (wl.page_table[idx] if wl.layout == synth.LAYOUT_DECODE else wl.page_table).cpu().numpy()
+    lens = wl.seq_len[idx].cpu().numpy()
     K, P = wl.topk_blocks, wl.topk
-    done, t_total = 0, 0.0
-    for i, t in enumerate(rows):
-        L = int(lens[t])
-        t0 = time.perf_counter()
-        src = O.source_row(layers[0], pts, wl.layout, i, L, max(K, P + 1), P)
+
+    def one(i):
+        L = int(lens[i])
+        src = O.source_row(layers[0], pt, wl.layout, i, L, max(K, P + 1), P)
         blocks, nv = O.select_blocks(src["keys"], O.num_blocks(L), K)
         for j in range(1, len(layers)):
-            O.select_row(layers[j], pts, wl.layout, i, L, blocks, nv, P)
-        t_total += time.perf_counter() - t0
-        done += 1
-        if t_total > budget_s:
-            break
-    del wl
-    torch.cuda.empty_cache() if torch.cuda.is_available() else None
-    per_row = t_total / done
-    threads = torch.get_num_threads()
-    try:
-        import threadpoolctl
+            O.select_row(layers[j], pt, wl.layout, i, L, blocks, nv, P)
 
-        info = threadpoolctl.threadpool_info()
-        if info:
-            threads = max(i.get("num_threads", 1) for i in info)
-    except Exception:
-        pass
-    return per_row * int(lens.shape[0]) * 1e3, done, threads, int(lens.shape[0])
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, range(len(rows))))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, unit, cap=128, threads=None):
+    """The oracle timed on the host cores over a bounded row sample of ``wl``
+    (all rows when there are at most ``cap``), in the line's unit: ms per step
+    extrapolated linearly to every row (rows are independent), or rows/s."""
+    threads = threads or host_threads()
+    rows = sample_rows(wl.rows, cap)
+    sec = oracle_rows_s(wl, rows, threads)
+    per_step_ms = sec * 1e3 * wl.rows / len(rows)
+    value = wl.rows / (per_step_ms * 1e-3) if unit == "rows/s" else per_step_ms
+    what = "all rows" if len(rows) == wl.rows else (f"{len(rows)} of {wl.rows} rows (first {cap // 4}, last "
+                                                    f"{cap // 4}, {cap // 2} evenly spaced), extrapolated linearly")
+    return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{what}; all {len(wl.layers)} layers; one row per host thread ({threads} threads), "
+                      f"{sec:.1f} s wall"}
+
+
+def headline_config(wl, world, kv="fp8"):
+    return {"workload": wl.name, "rows": wl.rows, "context": wl.max_len, "topk_blocks": wl.topk_blocks,
+            "topk": wl.topk, "layers": len(wl.layers), "index_k": kv, "parallelism": f"replicas x{world}",
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+REFERENCE_ROWS_PER_STEP = 48
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands, on the host cores, timed on
+    the headline workload.  Each step is a bounded row sample (the first,
+    last and evenly spaced rows, REFERENCE_ROWS_PER_STEP of them) extrapolated
+    linearly to the chunk."""
     world, rank, local = dist_env()
     if rank != 0:
         return 0
-    ms_per_step, done, threads, nrows = cpu_oracle_sample(HEADLINE_CID, budget_s=15.0)
+    from two_level_sparse_gb300 import synth
+
+    kv = getattr(args, "kv", "fp8")
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = synth.config_workload(HEADLINE_CID, device=dev, kv=1 if kv == "mxfp4" else 0)
+    threads = host_threads()
+    rows = sample_rows(wl.rows, REFERENCE_ROWS_PER_STEP)
     steps = []
     for _ in range(args.warmup + args.steps):
-        m, done, threads, nrows = cpu_oracle_sample(HEADLINE_CID, budget_s=5.0)
-        steps.append(m)
-    value = statistics.mean(steps[args.warmup:]) if args.steps else ms_per_step
-    sample = f"{done} of {nrows} rows per step, timed and extrapolated linearly to the chunk"
+        steps.append(oracle_rows_s(wl, rows, threads) * 1e3 * wl.rows / len(rows))
+    value = statistics.mean(steps[args.warmup:]) if args.steps else steps[-1]
+    sample = (f"{len(rows)} of {wl.rows} rows per step (first, last and evenly spaced), all {len(wl.layers)} "
+              f"layers, one row per host thread, extrapolated linearly to the chunk")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill_16384rows_ctx262144_K2048", "rows": 16384, "context": 262144,
-                   "topk_blocks": 2048, "topk": 512, "layers": 5},
+        "config": headline_config(wl, world, kv),
         "cpu_baseline": {"value": value, "unit": "ms", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -336,32 +408,48 @@ def measure(cid, steps, warmup, stream, flush, e2e=False, rows=0, wl=None, kv=0)
     return res
 
 
-def measure_mxfp4(steps, stream, flush, world, peaks):
+def measure_mxfp4(steps, stream, flush, world, peaks, peak_src):
     """The headline chunk with MXFP4 index-K pools (the pages' use_fp4_cache
-    variant): the same step with FP4 x FP4 block-scaled MMAs and 68-byte K
-    positions."""
+    variant): the same step with FP4 x FP4 block-scaled MMAs (kind::mxf4) and
+    68-byte K positions."""
     from two_level_sparse_gb300 import synth
 
     wl = synth.config_workload(HEADLINE_CID, device="cuda", kv=synth.KV_MXFP4)
     r = measure(None, steps, 3, stream, flush, wl=wl)
     mst, msd, mss = (statistics.mean(r[k]) for k in ("t_step", "t_dense", "t_select"))
     flops, _, _ = algorithmic_counts(wl)
-    sel = select_bytes(wl)
-    fp4_peak = 4.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    positions, gathered, _ = select_work(wl)
+    fp4_peak, fp4_src = tensor_peaks(peaks, peak_src)["fp4"]
     line = {
         "metric": "indexer ms per 16K-token prefill chunk @262K ctx, MXFP4 index-K", "workload": wl.name,
         "value": mst, "unit": "ms", "ms_per_step": mst,
         "kernel_ms": {"dense": msd, "publish": statistics.mean(r["t_publish"]), "select": mss},
-        "dense_roofline": {"bound": "tensor", "achieved": flops / (msd * 1e-3) / 1e12, "peak": fp4_peak,
-                           "unit": "TFLOP/s", "frac": flops / (msd * 1e-3) / 1e12 / fp4_peak,
-                           "peak_source": "bf16_tflops_sustained x4 (fp4 / bf16 nominal ratio)"},
-        "select_roofline": {"bound": "hbm", "achieved": sel / (mss * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                            "unit": "GB/s", "frac": sel / (mss * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                            "bytes_per_step": sel},
+        "dense_roofline": tensor_roofline(flops, msd, 1, fp4_peak, fp4_src),
+        "select_roofline": tensor_roofline(2 * 64 * 128 * positions, mss, len(wl.layers), fp4_peak, fp4_src),
+        "l2_gather": l2_gather(gathered, mss),
         "dev_err": int(r["step"].dev_err.item()),
     }
     del r
     return line
+
+
+def tensor_roofline(flops_per_step, ms_per_step, launches, peak, peak_source, kernel=None, traffic=None):
+    """A scorer against its block-scaled tensor peak: flops per launch over the
+    mean launch time (launches that overlap at their edges on side streams
+    count the phase / launches)."""
+    achieved = flops_per_step / (ms_per_step * 1e-3) / 1e12
+    out = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+           "traffic": traffic, "peak_source": peak_source, "flops_per_launch": flops_per_step / launches,
+           "launches_per_step": launches, "ms_per_launch": ms_per_step / launches, "ms_per_step": ms_per_step}
+    if kernel:
+        out = {"kernel": kernel, **out}
+    return out
+
+
+def l2_gather(gathered_bytes, ms):
+    return {"gbs": gathered_bytes / (ms * 1e-3) / 1e9, "bytes_per_step": gathered_bytes,
+            "note": "candidate index-K gathered by the selects; a prefill chunk's pools (34.6 MB per layer) "
+                    "are L2-resident, so these bytes come from L2 and are not a fraction of HBM bandwidth"}
 
 
 def measure_dcp(steps, stream, flush, world):
@@ -516,7 +604,7 @@ def main():
         steps = max(1, args.steps)
         one = {"qprod": lambda: measure_qprod(steps, stream, flush, peaks),
                "varlen": lambda: measure_varlen(steps, stream, flush, world),
-               "mxfp4": lambda: measure_mxfp4(steps, stream, flush, world, peaks),
+               "mxfp4": lambda: measure_mxfp4(steps, stream, flush, world, peaks, peak_src),
                "dcp": lambda: measure_dcp(steps, stream, flush, 2)}[args.only]()
         emit_line(one, rank)
         if world > 1:
@@ -539,78 +627,51 @@ def main():
     wl = head["wl"]
     err = int(head["step"].dev_err.item())
     flops, kbytes, positions = algorithmic_counts(wl)
-    fp8_peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    achieved = flops / (ms_dense * 1e-3) / 1e12
-    sel_bytes = select_bytes(wl)
+    tpk = tensor_peaks(peaks, peak_src)
+    peak, peak_source = tpk["fp4" if args.kv == "mxfp4" else "fp8"]
+    sel_positions, sel_gathered, _ = select_work(wl)
     n_select = len(wl.layers)
-    sel_gbs = sel_bytes / (ms_select * 1e-3) / 1e9
     e2e_ms, h2d, d2h = head.get("e2e", ([float("nan")], 0, 0))
     e2e_val = statistics.mean(e2e_ms)
     (e2e_val,) = max_over_ranks([e2e_val], world, "cuda")
+    cpu_head = None
+    if rank == 0 and not args.no_cpu:
+        cpu_head = cpu_baseline(wl, "ms")
+    config = headline_config(wl, world, args.kv)
+    del head
+    torch.cuda.empty_cache()
 
     secondary = []
     if not args.no_secondary:
-        del head
-        torch.cuda.empty_cache()
-        for cid in (2, 1, 0):
-            r = measure(cid, max(3, args.steps // 2), 3, stream, flush)
-            mst = statistics.mean(r["t_step"])
-            msd = statistics.mean(r["t_dense"])
-            mss = statistics.mean(r["t_select"])
-            msg = graph_step_ms(r["step"], max(3, args.steps // 2), stream, flush)
-            f, b, _ = algorithmic_counts(r["wl"])
-            sb = select_bytes(r["wl"])
-            rows = r["wl"].rows
-            secondary.append({
-                "metric": "decode rows/s", "workload": r["wl"].name, "value": world * rows / (mst * 1e-3),
-                "unit": "rows/s", "ms_per_step": mst, "dense_ms": msd,
-                "graph": {"ms_per_step": msg, "rows_per_s": world * rows / (msg * 1e-3),
-                          "note": "the same step replayed as a CUDA graph"},
-                "dense_roofline": {"bound": "hbm", "achieved": b / (msd * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                                   "unit": "GB/s", "frac": b / (msd * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-                "select_roofline": {"bound": "hbm", "achieved": sb / (mss * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                                    "unit": "GB/s", "frac": sb / (mss * 1e-3) / 1e9 / peaks["hbm_gbs"], "ms": mss,
-                                    "launches": r["launches"] - 2,
-                                    "note": "candidate K gathered by the five layers' selects (pools larger than L2: "
-                                            "from HBM) / select time"},
-                "dev_err": int(r["step"].dev_err.item()),
-            })
-            del r
+        for cid in (3, 2, 1, 0):
+            secondary.append(measure_secondary(cid, args, stream, flush, world, rank, peaks, tpk))
             torch.cuda.empty_cache()
         secondary.append(measure_varlen(max(3, args.steps // 2), stream, flush, world))
         torch.cuda.empty_cache()
-        secondary.append(measure_mxfp4(max(3, args.steps // 2), stream, flush, world, peaks))
+        secondary.append(measure_mxfp4(max(3, args.steps // 2), stream, flush, world, peaks, peak_src))
         torch.cuda.empty_cache()
         secondary.append(measure_qprod(max(3, args.steps // 2), stream, flush, peaks))
         torch.cuda.empty_cache()
         secondary.append(measure_dcp(3, stream, flush, 2))
         torch.cuda.empty_cache()
 
-    cpu_ms, cpu_rows, cpu_threads, nrows = (None, 0, 0, 0)
-    if rank == 0 and not args.no_cpu:
-        cpu_ms, cpu_rows, cpu_threads, nrows = cpu_oracle_sample(HEADLINE_CID, budget_s=15.0)
     value = ms_step / world
+    dense_rl = tensor_roofline(flops, ms_dense, 1, peak, peak_source, kernel="dense_amax8_kernel",
+                               traffic=recorded_traffic("dense_amax8_kernel"))
+    dense_rl["peak_mxf8f6f4_probe"] = MXF8F6F4_PROBE_TFLOPS
+    dense_rl["frac_of_probe"] = dense_rl["achieved"] / MXF8F6F4_PROBE_TFLOPS
+    select_rl = tensor_roofline(2 * 64 * 128 * sel_positions, ms_select, n_select, peak, peak_source,
+                                kernel="select_kernel", traffic=recorded_traffic("select_kernel"))
+    select_rl["l2_gather"] = l2_gather(sel_gathered, ms_select)
     line = {
         "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": value / PAGES_LAST_CHUNK_MS, "dtype": "e4m3xe4m3->f32 (mxf8f6f4, ue8m0 scales)",
+        "vs_baseline": value / PAGES_LAST_CHUNK_MS,
+        "dtype": ("e2m1xe2m1->f32 (mxf4, ue8m0 scales)" if args.kv == "mxfp4"
+                  else "e4m3xe4m3->f32 (mxf8f6f4, ue8m0 scales)"),
         "data": "synthetic",
-        "config": {"workload": wl.name, "rows": wl.rows, "context": wl.max_len,
-                   "topk_blocks": 2048, "topk": 512, "layers": 5, "index_k": args.kv, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (256 MiB write)"},
-        **rooflines(
-            {"bound": "tensor", "kernel": "dense_amax8_kernel", "achieved": achieved, "peak": fp8_peak,
-             "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": recorded_traffic("dense_amax8_kernel"),
-             "peak_source": f"{peak_src} bf16_tflops_sustained x2 (fp8 / bf16 nominal ratio)",
-             "flops_per_launch": flops, "launches_per_step": 1, "ms_per_launch": ms_dense, "ms_per_step": ms_dense},
-            {"bound": "hbm", "kernel": "select_kernel", "achieved": sel_gbs, "peak": peaks["hbm_gbs"],
-             "unit": "GB/s", "frac": sel_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("select_kernel"),
-             "peak_source": f"{peak_src} hbm_gbs",
-             "bytes_per_launch": sel_bytes / n_select, "launches_per_step": n_select,
-             "ms_per_launch": ms_select / n_select, "ms_per_step": ms_select,
-             "note": "candidate K gathered per launch (132 B per position) / mean launch time (the five "
-                     "launches run on side streams and overlap at their edges: the select phase / 5); "
-                     "for a prefill chunk the 34.6 MB pool per layer is L2-resident"}),
+        "config": config,
+        **rooflines(dense_rl, select_rl),
         "kernel_ms": {"dense": ms_dense, "publish": ms_publish, "select": ms_select},
         "e2e": {"value": e2e_val / world, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": head_launches(args.steps, world),
@@ -618,14 +679,56 @@ def main():
         "wall_s": wall,
         "dev_err": err,
         "secondary": secondary,
-        "cpu_baseline": None if cpu_ms is None else {
-            "value": cpu_ms, "unit": "ms", "cores": cpu_threads, "kind": "oracle",
-            "sample": f"{cpu_rows} of {nrows} rows (last, first, middle), all 5 layers, extrapolated linearly"},
+        "cpu_baseline": cpu_head,
     }
     emit_line(line, rank)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def measure_secondary(cid, args, stream, flush, world, rank, peaks, tpk):
+    """One of the standard workloads beside the headline chunk: the decode
+    batches (rows/s, HBM-bound: their pools exceed L2) and the 4096-row
+    prefill chunk (every row keeps all its blocks: the five layers score
+    every position, tensor-bound), each with the oracle's CPU baseline."""
+    r = measure(cid, max(3, args.steps // 2), 3, stream, flush)
+    wl = r["wl"]
+    mst, msd, mss = (statistics.mean(r[k]) for k in ("t_step", "t_dense", "t_select"))
+    msg = graph_step_ms(r["step"], max(3, args.steps // 2), stream, flush)
+    f, b, _ = algorithmic_counts(wl)
+    positions, gathered, other = select_work(wl)
+    rows = wl.rows
+    line = {"workload": wl.name, "ms_per_step": mst, "dense_ms": msd, "select_ms": mss,
+            "graph": {"ms_per_step": msg, "rows_per_s": world * rows / (msg * 1e-3),
+                      "note": "the same step replayed as a CUDA graph"}}
+    if wl.layout == 0:
+        line = {"metric": "decode rows/s", "value": world * rows / (mst * 1e-3), "unit": "rows/s", **line}
+        if cid != 0:  # the 4-row batch is latency-bound: no roofline claim
+            hbm = peaks["hbm_gbs"]
+            line["dense_roofline"] = {"bound": "hbm", "achieved": b / (msd * 1e-3) / 1e9, "peak": hbm,
+                                      "unit": "GB/s", "frac": b / (msd * 1e-3) / 1e9 / hbm, "bytes": b}
+            sb = gathered + other
+            line["select_roofline"] = {"bound": "hbm", "achieved": sb / (mss * 1e-3) / 1e9, "peak": hbm,
+                                       "unit": "GB/s", "frac": sb / (mss * 1e-3) / 1e9 / hbm, "bytes": sb,
+                                       "launches": r["launches"] - 2,
+                                       "note": "candidate K gathered by the five layers' selects (pools larger "
+                                               "than L2: from HBM) plus per-row bytes / select time"}
+            line["step_roofline"] = {"bound": "hbm", "achieved": (b + sb) / (mst * 1e-3) / 1e9, "peak": hbm,
+                                     "unit": "GB/s", "frac": (b + sb) / (mst * 1e-3) / 1e9 / hbm}
+        unit = "rows/s"
+    else:
+        peak, src = tpk["fp8"]
+        line = {"metric": "prefill chunk ms", "value": mst, "unit": "ms", "rows_per_s": world * rows / (mst * 1e-3),
+                **line}
+        line["select_roofline"] = tensor_roofline(2 * 64 * 128 * positions, mss, len(wl.layers), peak, src)
+        line["l2_gather"] = l2_gather(gathered, mss)
+        unit = "ms"
+    line["dev_err"] = int(r["step"].dev_err.item())
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, unit)
+    del r
+    return line
 
 
 def rooflines(a, b):
