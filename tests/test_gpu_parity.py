@@ -251,6 +251,61 @@ def test_publish_pair_equals_two_single_publishes(ci, K1, K2):
             assert np.all(out[t, nv:] == 0x7FFFFFFF)
 
 
+def _publish_rows_against_oracle(ci, keys, lens, K1, K2):
+    """ci_publish_blocks2 on the given keys against the oracle's selection."""
+    rows, stride = keys.shape
+    max_len = int(lens.max())
+    dev = "cuda"
+    kd, ld = keys.to(dev).contiguous(), lens.to(dev)
+    b1 = torch.full((rows, K1), -5, dtype=torch.int32, device=dev)
+    n1 = torch.empty(rows, dtype=torch.int32, device=dev)
+    b2 = torch.full((rows, K2), -5, dtype=torch.int32, device=dev)
+    n2 = torch.empty(rows, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ci.ci_publish_blocks2(ld, max_len, kd, K1, b1, n1, K2, b2, n2, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    b1h, b2h, n1h, n2h = b1.cpu().numpy(), b2.cpu().numpy(), n1.cpu().numpy(), n2.cpu().numpy()
+    for t in range(rows):
+        nb = O.num_blocks(int(lens[t]))
+        kr = keys[t, :nb].double().numpy()
+        for K, out, nv_out in ((K1, b1h, n1h), (K2, b2h, n2h)):
+            ids, nv = O.select_blocks(kr, nb, K)
+            assert int(nv_out[t]) == nv
+            assert np.array_equal(out[t, :nv], ids[:nv]), (t, K)
+            assert np.all(out[t, nv:] == 0x7FFFFFFF)
+
+
+@needs_cuda
+@pytest.mark.parametrize("case", ["normal", "ties", "sample_adversarial", "mid_length", "wider_second"])
+def test_publish_long_rows_match_the_oracle(ci, case):
+    """Rows of thousands of blocks, whose threshold the publish kernel brackets
+    from a strided sample of the keys (with the radix path behind it when the
+    sample's bound misses): the oracle's selection, ties toward the lower id,
+    in every case -- random keys, keys with heavy ties at the threshold, keys
+    whose every sampled position (each 16th block) outranks all the others so
+    that the sample's bound fails, rows of 4096 - 8192 blocks, and a second
+    selection wider than the first."""
+    g = torch.Generator().manual_seed(91)
+    rows = 24
+    L = 262144
+    lens = torch.full((rows,), L, dtype=torch.int32)
+    lens[1] = L - 5  # a ragged newest block
+    K1, K2 = 2048, 513
+    if case == "mid_length":
+        lens = torch.randint(8 * 4096, 8 * 8192, (rows,), generator=g, dtype=torch.int32)
+    stride = ((int(lens.max()) + 7) // 8 + 7) // 8 * 8
+    keys = torch.randn(rows, stride, generator=g)
+    if case == "ties":
+        keys = torch.round(keys * 3.0) / 3.0  # a handful of distinct values: long runs of ties at the threshold
+    elif case == "sample_adversarial":
+        keys[:, ::16] += 50.0
+    elif case == "wider_second":
+        K1, K2 = 128, 513
+    keys[2, : stride // 2] = -float("inf")
+    _publish_rows_against_oracle(ci, keys, lens, K1, K2)
+
+
 
 @needs_cuda
 @pytest.mark.parametrize("cid", [1, 3])

@@ -23,11 +23,10 @@
 //               tile's K scale factors and two kind::mxf4 steps of K = 64;
 //   warps 1-3   gather a tile's 16 candidate blocks (each contiguous K in its
 //               page: 1 KB FP8, 512 B MXFP4) into a swizzled MMA tile of a
-//               9-deep ring: warp 1 with 8-row tensor-map loads for 6 (MXFP4:
-//               8) of them, warps 2-3 with 16-byte cp.async for the others
-//               (each path alone is capped well below what both reach
-//               together); for MXFP4 warps 2-3 also stage the 128 positions'
-//               scale words for the MMA warp's tcgen05.cp;
+//               9-deep ring with 16-byte cp.async from every lane (warp g
+//               takes blocks g, g + 3, ...), each lane arriving on the tile's
+//               barrier once its copies have landed; for MXFP4 they also stage
+//               the 128 positions' scale words for the MMA warp's tcgen05.cp;
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
 //               then, two rows ahead, the page of every candidate block, the
 //               query (widened from e2m1 to e4m3 against FP8 K, packed against
@@ -55,14 +54,7 @@ constexpr int kSfa4Col = 480;     // MXFP4 K: 4 columns of A scale factors per a
 constexpr int kBlocksPerTile = kTileM / kBlock;  // 16
 constexpr int kMaxBlocks = 2176;                 // >= topk + 1 for every supported topk
 constexpr int kMaxTiles = kMaxBlocks / kBlocksPerTile;  // 136
-constexpr int kGatherWarp0 = 1, kGatherWarps = 3;  // warp 1 tensor-map loads, warps 2-3 cp.async
-// Blocks of a tile fetched by tensor-map loads, the rest by cp.async: the
-// split that balances the two paths (measured: FP8 1 KB blocks 6, MXFP4
-// 512-byte blocks 8).
-template <int KV>
-__host__ __device__ constexpr int tma_blocks() {
-  return KV == kKvMxfp4 ? 8 : 6;
-}
+constexpr int kGatherWarp0 = 1, kGatherWarps = 3;  // cp.async gatherers
 constexpr int kTopkWarp0 = 4, kTopkThreads = 128, kTopkBar = 2;  // also the next-row prep
 constexpr int kPrepThreads = kTopkThreads;
 constexpr int kScoreWarp0 = 8;
@@ -81,7 +73,7 @@ struct __align__(1024) Smem {
   // gathered A tiles (1024-aligned); MXFP4 tiles take the first 8 KB of a slot
   // and stage their scale factors for tcgen05.cp at byte 8192 of it
   uint8_t kv[kStages][kTileM * kDim];
-  uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered
+  uint8_t q[2][kHeads * kDim];         // widened queries, double-buffered (1024-aligned: swizzled B tiles)
   uint8_t sf[2][512];                  // query scale factors staged for tcgen05.cp
   // per candidate: (page << 10) | (8-position group in the page << 7) |
   // (first position in the group << 4) | positions below L (1..8), or -1
@@ -90,7 +82,7 @@ struct __align__(1024) Smem {
   uint4 mgt[kMaxTiles], meq[kMaxTiles];  // top-k compaction ballots, one word per warp
   int gbase[kMaxTiles], ebase[kMaxTiles];  // top-k: entries above / at the threshold before each tile
   int scan_part[2][kTopkThreads / 32];
-  uint64_t k_full[kStages], tk_full[kStages], k_empty[kStages];
+  uint64_t k_full[kStages], k_empty[kStages];
   uint64_t t_full[kNumAcc], t_empty[kNumAcc];
   uint64_t q_full[2], q_empty[2];
   uint64_t info_full[2], info_empty[2];
@@ -105,6 +97,8 @@ struct __align__(1024) Smem {
   TopkShared topk;
 };
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
+static_assert(offsetof(Smem, q) % 1024 == 0 && offsetof(Smem, kv) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(offsetof(Smem, sf) % 16 == 0, "tcgen05.cp needs 16-byte alignment");
 
 __device__ __forceinline__ void set_abort(Smem& sm, int32_t* dev_err) {
   sm.abort_flag = 1;
@@ -507,18 +501,11 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   }
 }
 
-// The layers' tensor maps over their pools (8-row boxes).
-struct SelectMaps {
-  CUtensorMap m[kMaxSelectLayers];
-};
-
 template <int KV, bool kMulti>
-__global__ void __launch_bounds__(kThreads, 1)
-    select_kernel(const __grid_constant__ SelectMaps maps, const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a) {
   constexpr bool kFp4 = KV == kKvMxfp4;
   constexpr int kBlockBytes = kBlock * row_bytes<KV>();  // one candidate block's values: 1 KB or 512 B
   constexpr int kPVB = page_value_bytes<KV>(), kPB = page_bytes<KV>();
-  constexpr int kTmaBlocks = tma_blocks<KV>();
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -530,8 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], 32 * (kGatherWarps - 1));  // one cp.async-tracked arrival per copying lane
-      mbar_init(&sm.tk_full[s], 1);                       // the tensor-map loads (transaction bytes)
+      mbar_init(&sm.k_full[s], 32 * kGatherWarps);  // every gather lane, once its copies of the tile landed
       mbar_init(&sm.k_empty[s], 1);
     }
     for (int s = 0; s < kNumAcc; ++s) {
@@ -550,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    for (int l = 0; l < a.num_layers; ++l) prefetch_tmap(&maps.m[l]);
   }
   tc_fence_before();
   __syncthreads();
@@ -590,7 +575,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int t = 0; t < r.ntiles; ++t) {
         if (!warp_wait_fast(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
-            !warp_wait_fast(&sm.tk_full[kr.idx], kr.phase, abort_flag) ||
             !warp_wait_fast(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -623,25 +607,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
     // ------------------------------------------------------------------ gather
-    // Random 1 KB gathers from L2 are capped per path: tensor-map loads by the
-    // rate one warp can issue them, cp.async by the copies the load/store unit
-    // keeps in flight.  Both paths run side by side: warp 1 issues tensor-map
-    // loads for the first kTmaBlocks blocks of a tile (one 8-row box each,
-    // landing on its own swizzle atom), warps 2-3 copy the other blocks with
-    // 16-byte cp.async.
+    // Every lane copies 16-byte chunks with cp.async (random 1 KB blocks from
+    // L2 or HBM: issued from all lanes, these reach several times the rate of
+    // one lane's tensor-map or bulk copies).  Warp gw takes blocks gw, gw + 3,
+    // ... of each tile; block blk is contiguous in its page and lands on its
+    // own 8-row swizzle atom.  Each lane then arrives on the tile's k_full as
+    // soon as its copies have landed (cp.async.mbarrier.arrive.noinc).
     const int gw = warp - kGatherWarp0;
     const uint32_t dst0 = sw128_offset(lane >> 3, (lane & 7) * 16), dst1 = sw128_offset(4 + (lane >> 3), (lane & 7) * 16);
-    Ring kr;
+    Ring kr;  // slot of the next tile to issue
     int ri = 0;
-    uint32_t issued = 0;  // warp 1: tiles whose tensor-map loads were issued
     bool ok = true;
     for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
       const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
-      const CUtensorMap* tmap = &maps.m[kMulti ? r.layer : 0];
       pin<kMulti>(k_pool);
-      pin<kMulti>(tmap);
       ok = warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t) {
@@ -651,62 +632,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* dst = sm.kv[kr.idx];
         const int row_base = t * kBlocksPerTile;
-        if (gw == 0) {
-          const int slot = row_base + lane;
-          const int v = lane < kTmaBlocks && slot < r.nv ? info[slot] : -1;
-          const uint32_t live = __ballot_sync(0xffffffffu, v >= 0);
-          mbar_arrive_expect_tx_elect(&sm.tk_full[kr.idx], __popc(live) * kBlockBytes);
+        const int my = lane < kBlocksPerTile && row_base + lane < r.nv ? info[row_base + lane] : -1;
 #pragma unroll
-          for (int blk = 0; blk < kTmaBlocks; ++blk) {
-            const int vb = __shfl_sync(0xffffffffu, v, blk);
-            if (vb >= 0)
-              tma_load_3d_elect(dst + blk * kBlockBytes, tmap, 0, ((vb >> 7) & 7) * kBlock, vb >> 10,
-                                &sm.tk_full[kr.idx]);
-          }
-          ++issued;
-        } else {
-          // block blk: contiguous in its page -> one 8-row swizzle atom;
-          // FP8 (1 KB): lane l copies 16-byte chunks l and l + 32 (rows l / 8
-          // and 4 + l / 8); MXFP4 (512 B): lane l copies chunk l (row l / 4)
-#pragma unroll 2
-          for (int blk = kTmaBlocks + gw - 1; blk < kBlocksPerTile; blk += kGatherWarps - 1) {
-            const int slot = row_base + blk;
-            const int v = slot < r.nv ? info[slot] : -1;
-            if (v >= 0) {
-              const uint8_t* src =
-                  k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
-              if (kFp4) {
-                cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
-              } else {
-                cp_async16(dst + blk * kBlockBytes + dst0, src);
-                cp_async16(dst + blk * kBlockBytes + dst1, src + 512);
-              }
+        for (int blk = gw; blk < kBlocksPerTile; blk += kGatherWarps) {
+          const int v = __shfl_sync(0xffffffffu, my, blk);
+          if (v >= 0) {
+            // FP8 (1 KB): lane l copies 16-byte chunks l and l + 32 (rows
+            // l / 8 and 4 + l / 8); MXFP4 (512 B): lane l copies chunk l (row l / 4)
+            const uint8_t* src =
+                k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
+            if (kFp4) {
+              cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
+            } else {
+              cp_async16(dst + blk * kBlockBytes + dst0, src);
+              cp_async16(dst + blk * kBlockBytes + dst1, src + 512);
             }
           }
-          if (kFp4) {
-            // the scale words of all 128 positions, staged for tcgen05.cp:
-            // position p = 32 c + l goes to byte 16 l + 4 c
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int p = (gw - 1) * 64 + 32 * j + lane;
-              const int slot = row_base + (p >> 3);
-              const int v = slot < r.nv ? info[slot] : -1;
-              if (v >= 0)
-                cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
-                          k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
-            }
-          }
-          cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         }
+        if (kFp4) {
+          // the scale words of all 128 positions, staged for tcgen05.cp:
+          // position p = 32 c + l goes to byte 16 l + 4 c
+          for (int p = gw * 32 + lane; p < kTileM; p += 32 * kGatherWarps) {
+            const int v = __shfl_sync(0xffffffffu, my, p >> 3);
+            if (v >= 0)
+              cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
+                        k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
+          }
+        }
+        cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         kr.next(kStages);
       }
       __syncwarp();
       if (ok) mbar_arrive(&sm.info_empty[b]);
-    }
-    if (gw == 0 && !ok && lane == 0) {
-      // no tensor-map load may still be writing when the CTA exits
-      for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        mbar_wait(&sm.tk_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
     }
     cp_async_wait<0>();
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
@@ -798,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool valid = v >= 0 && (p & 7) >= off && (p & 7) < off + (v & 15);
           // this position's K scale, fetched now and used after the head sum
           // (MXFP4: 1, the scales are inside the MMA)
-          float kscale = kFp4 ? 1.0f : 0.0f;
+          float kscale = 1.0f;
           if (!kFp4 && valid)
             kscale = __ldg(reinterpret_cast<const float*>(k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB) +
                            ((v >> 7) & 7) * kBlock + (p & 7));
@@ -860,14 +817,9 @@ cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
   const int smem = static_cast<int>(select_smem_bytes(0));
   cudaError_t e = cudaFuncSetAttribute(select_kernel<KV, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  SelectMaps maps;
-  for (int l = 0; l < a.num_layers; ++l) {
-    e = make_pool_tmap(&maps.m[l], a.layer[l].k_pool, a.p.num_pages, KV, kBlock);
-    if (e != cudaSuccess) return e;
-  }
   const int64_t units = static_cast<int64_t>(a.num_layers) * a.p.rows;
   const int grid = units < device_sm_count() ? static_cast<int>(units) : device_sm_count();
-  select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(maps, a);
+  select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
