@@ -661,6 +661,16 @@ def test_dcp_full_size_prefill_chunk_sampled_rows(ci):
 
 
 @needs_cuda
+def test_decode_batch_all_rows(ci):
+    """The 64-row decode batch at full size against the oracle on every row."""
+    wl_dev = synth.config_workload(1, device="cuda")
+    step = run_step(None, wl_dev=wl_dev)
+    assert int(step.dev_err.item()) == 0
+    rows = list(range(wl_dev.rows))
+    assert_ok(compare.check_step(subset_workload(wl_dev, rows), step.outputs_numpy()))
+
+
+@needs_cuda
 @pytest.mark.parametrize("case", ["decode", "prefill"])
 def test_select_layers_equals_one_launch_per_layer(ci, case):
     """One ci_select_sparse_layers launch over every layer (the source with
