@@ -202,6 +202,17 @@ def select_bytes(wl):
     return gathered + other
 
 
+def publish_bytes(wl):
+    """Algorithmic bytes of the publish launch: 4 per key of every row that
+    selects (nb_t > min(K, P + 1)), and the two tables it writes (K and
+    P + 1 ids, and a count, per row)."""
+    L = wl.seq_len.to(torch.int64).cpu()
+    nb = (L + 7) // 8
+    K, Kp = wl.topk_blocks, wl.topk + 1
+    reads = int((4 * nb[nb > min(K, Kp)]).sum())
+    return reads + wl.rows * 4 * (K + Kp + 2)
+
+
 def time_steps(step, steps, warmup, flush, stream, dense_events=True):
     """Per-step CUDA-event durations (ms) on `stream`, whole step and per
     kernel kind (events recorded between the step's launches)."""
@@ -576,7 +587,8 @@ def main():
                     help="keep only the last ROWS rows of the headline chunk (a smaller case for profilers)")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "mxfp4"],
                     help="index-K page format of the headline chunk (the reported metric is defined on fp8)")
-    ap.add_argument("--only", default=None, choices=["qprod", "varlen", "mxfp4", "dcp"],
+    ap.add_argument("--only", default=None,
+                    choices=["qprod", "varlen", "mxfp4", "dcp", "decode4", "decode64", "decode128", "prefill4096"],
                     help="run one secondary workload alone and print its line (a small command for profilers)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -602,10 +614,16 @@ def main():
 
     if args.only is not None:
         steps = max(1, args.steps)
-        one = {"qprod": lambda: measure_qprod(steps, stream, flush, peaks),
-               "varlen": lambda: measure_varlen(steps, stream, flush, world),
-               "mxfp4": lambda: measure_mxfp4(steps, stream, flush, world, peaks, peak_src),
-               "dcp": lambda: measure_dcp(steps, stream, flush, 2)}[args.only]()
+        tpk = tensor_peaks(peaks, peak_src)
+        std = {"decode4": 0, "decode64": 1, "decode128": 2, "prefill4096": 3}
+        if args.only in std:
+            args.no_cpu = True
+            one = measure_secondary(std[args.only], args, stream, flush, world, rank, peaks, tpk)
+        else:
+            one = {"qprod": lambda: measure_qprod(steps, stream, flush, peaks),
+                   "varlen": lambda: measure_varlen(steps, stream, flush, world),
+                   "mxfp4": lambda: measure_mxfp4(steps, stream, flush, world, peaks, peak_src),
+                   "dcp": lambda: measure_dcp(steps, stream, flush, 2)}[args.only]()
         emit_line(one, rank)
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -663,6 +681,10 @@ def main():
     select_rl = tensor_roofline(2 * 64 * 128 * sel_positions, ms_select, n_select, peak, peak_source,
                                 kernel="select_kernel", traffic=recorded_traffic("select_kernel"))
     select_rl["l2_gather"] = l2_gather(sel_gathered, ms_select)
+    pub_b = publish_bytes(wl)
+    publish_rl = {"bound": "hbm", "kernel": "publish_kernel", "achieved": pub_b / (ms_publish * 1e-3) / 1e9,
+                  "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": pub_b / (ms_publish * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "traffic": recorded_traffic("publish_kernel"), "bytes_per_launch": pub_b, "ms_per_launch": ms_publish}
     line = {
         "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
@@ -672,6 +694,7 @@ def main():
         "data": "synthetic",
         "config": config,
         **rooflines(dense_rl, select_rl),
+        "roofline_publish": publish_rl,
         "kernel_ms": {"dense": ms_dense, "publish": ms_publish, "select": ms_select},
         "e2e": {"value": e2e_val / world, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": head_launches(args.steps, world),
@@ -742,12 +765,15 @@ def rooflines(a, b):
 # at full size (one-pass metrics), with the hash of the kernel's sources; a
 # figure is reported only while the sources still match.
 RECORDED_TRAFFIC = {
-    # mean of the five launches of a step (source 170.6 MB, consumers 273.0-273.9 MB)
+    # mean of the five launches of a step: 225.7 MB read (the pool once, queries, ids) + 27.2 MB written
     "select_kernel": {"bytes_per_launch": 252.9e6, "sources": ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
-                      "sha256": "ce701e938199b9979c131f1616068fde9dd6211d8e20783cd96b97262f9b6612"},
-    # 129.2 MB read (pool, queries) + 2038.0 MB written (keys)
-    "dense_amax8_kernel": {"bytes_per_launch": 2167.2e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
-                           "sha256": "7405a49da0a8f885945c6f8d05467c7ce6d7474b23e8d87d4e70fbc3111e2516"},
+                      "sha256": "d3a6d98222cea446a23dca54c566f52a6bba8cf3ac6721adf45aef0fca4d4dff"},
+    # 130.7 MB read (pool, queries) + 2037.5 MB written (keys)
+    "dense_amax8_kernel": {"bytes_per_launch": 2168.2e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+                           "sha256": "8709d863167b7fba76fc6fdb72220b7632922a8338a886d94ea0f999b1260c41"},
+    # 2083.1 MB read (keys) + 166.5 MB written (the two tables)
+    "publish_kernel": {"bytes_per_launch": 2249.6e6, "sources": ("publish.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+                       "sha256": "f77f256923267887c63b60881cf5557d961b7446cda328033c182780c92e5e87"},
 }
 
 
