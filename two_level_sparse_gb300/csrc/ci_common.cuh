@@ -87,6 +87,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+// Bounded wait by lane 0 alone, the verdict broadcast and the warp
+// synchronized after it (its memory ordering carries lane 0's acquire to the
+// other lanes): for warps whose lanes then only write shared memory or whose
+// work is issued by one elected lane, one probe per wait instead of 32.
+__device__ __forceinline__ bool warp_wait_lane0(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
 // The common case first: every lane probes once and the warp votes; only when
 // the phase is not complete yet does it fall back to the bounded wait.
 __device__ __forceinline__ bool warp_wait_fast(uint64_t* bar, uint32_t parity, volatile int* abort) {

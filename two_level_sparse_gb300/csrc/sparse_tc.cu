@@ -574,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
         idesc[k] = kFp4 ? idesc_mxf4(kTileM, kHeads, 2 * (k & 1), 2 * (k & 1)) : idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
       }
       for (int t = 0; t < r.ntiles; ++t) {
-        if (!warp_wait_fast(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
-            !warp_wait_fast(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
+        if (!warp_wait_lane0(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
+            !warp_wait_lane0(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -623,10 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
       const int b = ri & 1;
       const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
       pin<kMulti>(k_pool);
-      ok = warp_wait(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
+      ok = warp_wait_lane0(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t) {
-        if (!warp_wait(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
+        if (!warp_wait_lane0(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
