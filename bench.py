@@ -765,14 +765,14 @@ def rooflines(a, b):
 # at full size (one-pass metrics), with the hash of the kernel's sources; a
 # figure is reported only while the sources still match.
 RECORDED_TRAFFIC = {
-    # mean of the five launches of a step: 225.7 MB read (the pool once, queries, ids) + 27.2 MB written
-    "select_kernel": {"bytes_per_launch": 252.9e6, "sources": ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+    # mean of the five launches of a step: 225.4 MB read (the pool once, queries, ids) + 27.2 MB written
+    "select_kernel": {"bytes_per_launch": 252.6e6, "sources": ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
                       "sha256": "ab9046fcf3f03cef10499ddbdfdedc42be8b5cb13034fe57ee26f76c60710ca7"},
-    # 130.7 MB read (pool, queries) + 2037.5 MB written (keys)
-    "dense_amax8_kernel": {"bytes_per_launch": 2168.2e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+    # 128.0 MB read (pool, queries) + 2037.6 MB written (keys)
+    "dense_amax8_kernel": {"bytes_per_launch": 2165.6e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
                            "sha256": "6480086ade7e6eda3a02fbed460ce32bc926c3f3aea1b65912eca55013eaf568"},
-    # 2083.1 MB read (keys) + 166.5 MB written (the two tables)
-    "publish_kernel": {"bytes_per_launch": 2249.6e6, "sources": ("publish.cu", "ci_common.cuh", "sm103_ptx.cuh"),
+    # 2082.5 MB read (keys) + 166.5 MB written (the two tables)
+    "publish_kernel": {"bytes_per_launch": 2249.0e6, "sources": ("publish.cu", "ci_common.cuh", "sm103_ptx.cuh"),
                        "sha256": "b4cafd48a0a5f090f4f7334b9e043fd616f6d47742141011f9108a57bf35216e"},
 }
 
