@@ -428,19 +428,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t col0 = R == 3 ? epi * kHeads : 0;
       const uint32_t ts0 = tseq;
       float* kp_row = keys_row != nullptr ? keys_row + (p >> 3) : nullptr;  // + 16 t per tile
-      for (int t = off; t < off + take; ++t) {
-        const uint32_t ts = ts0 + (t - off);
-        if (R == 1 && static_cast<int>(ts % 3) != epi) continue;
-        const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
+      // per-warp bases: this warp's tensor-memory lanes and columns, its scale
+      // word in slot 0 of the scale ring
+      const uint32_t tq = tmem_addr(tbase, 32 * quad, col0);
+      const uint32_t ks0 = smem_u32(&sm.ks[0][p]);
+      // One tile: accumulator stage ai (a compile-time constant where the
+      // caller knows it), phases from the tile's sequence number ts.
+      auto tile = [&](int t, uint32_t ts, uint32_t ai) -> bool {
+        const uint32_t ap = (ts / kNumAcc) & 1;
         const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
         if (!warp_wait_fast(&sm.t_full[ai], ap, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
-          break;
+          return false;
         }
         tc_fence_after();
         HeadAcc part = {{0, 0, 0, 0}};
         uint32_t x[32];
-        const uint32_t taddr = tmem_addr(tbase, 32 * quad, ai * N + col0);
+        const uint32_t taddr = tq + ai * N;
         tmem_ld32(taddr, x);
         tmem_ld_wait();
         head_reduce_half(part, x, w2);
@@ -455,9 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!kFp4) {
           if (!warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
             if (lane == 0) set_abort(sm, a.p.dev_err);
-            break;
+            return false;
           }
-          kscale = sm.ks[si][p];
+          kscale = lds_f32(ks0 + si * (kTileM * 4));
         }
         if (kScaleRelease) {
           __syncwarp();
@@ -477,6 +481,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
           if ((lane & 7) == 0 && pos < rlen)
             kp_row[t * (kTileM / kBlock)] = (pos >> 3) == nb - 1 ? __int_as_float(0x7f800000) : v;
+        }
+        return true;
+      };
+      const int end = off + take;
+      if (R == 3) {
+        // two accumulator stages: tiles in pairs, stage 0 then stage 1, so
+        // that every stage-dependent address is a constant of its copy
+        int t = off;
+        bool ok = true;
+        if ((ts0 & 1) && t < end) {
+          ok = tile(t, ts0, 1);
+          ++t;
+        }
+        for (; ok && t + 1 < end; t += 2) {
+          const uint32_t ts = ts0 + (t - off);
+          ok = tile(t, ts, 0) && tile(t + 1, ts + 1, 1);
+        }
+        if (ok && t < end) ok = tile(t, ts0 + (t - off), 0);
+      } else {
+        for (int t = off; t < end; ++t) {
+          const uint32_t ts = ts0 + (t - off);
+          if (static_cast<int>(ts % 3) != epi) continue;  // round-robin warpgroups
+          if (!tile(t, ts, ts & (kNumAcc - 1))) break;
         }
       }
     }
