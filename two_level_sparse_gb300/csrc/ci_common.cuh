@@ -129,11 +129,40 @@ __device__ __forceinline__ void relu_fma_pair(unsigned long long& acc, unsigned 
       : "+l"(acc), "+r"(x0), "+r"(x1)
       : "l"(w2));
 }
+// The same with the ReLU on the FMA pipe: x + |x| = 2 ReLU(x) exactly, so
+// the partial sums carry twice the values of the max form, each rounding
+// scaled by two as well, and the finish halves them exactly -- the same bits
+// wherever no partial sum is subnormal (|sum| < 2^-126).  Every kernel scoring
+// one K format uses one form (scorer_relu_abs_add below), which keeps the
+// dense keys and the sparse rescoring bit-identical in every case.
+__device__ __forceinline__ void relu2_fma_pair(unsigned long long& acc, unsigned long long w2, uint32_t& x0,
+                                               uint32_t& x1) {
+  asm("{\n\t.reg .b64 c;\n\t.reg .f32 a0, a1;\n\t"
+      "abs.f32 a0, %1;\n\tabs.f32 a1, %2;\n\t"
+      "add.rn.f32 %1, %1, a0;\n\tadd.rn.f32 %2, %2, a1;\n\t"
+      "mov.b64 c, {%1, %2};\n\tfma.rn.f32x2 %0, %3, c, %0;\n\t}"
+      : "+l"(acc), "+r"(x0), "+r"(x1)
+      : "l"(w2));
+}
+// ReLU form per K format: max.f32 (ALU pipe) for FP8 pools, x + |x| (FMA
+// pipe) for MXFP4 pools, whose scorers are shorter of FMA work and longer of
+// ALU work (the faster choice of each, by measurement).
+template <int KV>
+__host__ __device__ constexpr bool scorer_relu_abs_add() {
+  return KV == kKvMxfp4;
+}
 // x: heads 32 half .. 32 half + 31 of the position; w2: their 16 weight pairs.
+template <bool kAbsAdd>
 __device__ __forceinline__ void head_reduce_half(HeadAcc& acc, uint32_t (&x)[32], const unsigned long long* w2) {
 #pragma unroll
-  for (int m = 0; m < 16; ++m) relu_fma_pair(acc.p[m & 3], w2[m], x[2 * m], x[2 * m + 1]);
+  for (int m = 0; m < 16; ++m) {
+    if (kAbsAdd)
+      relu2_fma_pair(acc.p[m & 3], w2[m], x[2 * m], x[2 * m + 1]);
+    else
+      relu_fma_pair(acc.p[m & 3], w2[m], x[2 * m], x[2 * m + 1]);
+  }
 }
+template <bool kAbsAdd>
 __device__ __forceinline__ float head_reduce_finish(const HeadAcc& acc) {
   float a[8];
 #pragma unroll
@@ -141,7 +170,8 @@ __device__ __forceinline__ float head_reduce_finish(const HeadAcc& acc) {
     a[2 * i] = __uint_as_float(static_cast<uint32_t>(acc.p[i]));
     a[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(acc.p[i] >> 32));
   }
-  return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  const float s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  return kAbsAdd ? 0.5f * s : s;
 }
 // The 64 head weights of a row (16-byte aligned) as 32 packed pairs.
 __device__ __forceinline__ void load_head_weights(unsigned long long (&w2)[32], const float* w) {

@@ -33,6 +33,8 @@
 // R = 1 (N = 64, six stages) and the three epilogue warpgroups take tiles
 // round-robin.  Work is the list of (row group, 128-position tile) pairs,
 // split evenly across the CTAs.
+#include <type_traits>
+
 #include "ci_common.cuh"
 #include "ci_internal.h"
 
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MXFP4 scales are read by the MMA warp, in order, before it issues tile u,
   // so they never need a release either.
   constexpr bool kScaleRelease = R != 3 && !kFp4;
+  constexpr bool kAbsAdd = scorer_relu_abs_add<KV>();  // ReLU form: identical to the sparse scorer's
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -434,7 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ks0 = smem_u32(&sm.ks[0][p]);
       // One tile: accumulator stage ai (a compile-time constant where the
       // caller knows it), phases from the tile's sequence number ts.
-      auto tile = [&](int t, uint32_t ts, uint32_t ai) -> bool {
+      // kIn (a compile-time flag): every position of the tile is below the
+      // row's length and its last block is not the newest, so neither the
+      // mask nor the +inf pin applies.
+      auto tile = [&](int t, uint32_t ts, uint32_t ai, auto interior) -> bool {
+        constexpr bool kIn = decltype(interior)::value;
         const uint32_t ap = (ts / kNumAcc) & 1;
         const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
         if (!warp_wait_fast(&sm.t_full[ai], ap, abort_flag)) {
@@ -447,14 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t taddr = tq + ai * N;
         tmem_ld32(taddr, x);
         tmem_ld_wait();
-        head_reduce_half(part, x, w2);
+        head_reduce_half<kAbsAdd>(part, x, w2);
         tmem_ld32(taddr + 32, x);
         tmem_ld_wait();
-        head_reduce_half(part, x, w2 + 16);
+        head_reduce_half<kAbsAdd>(part, x, w2 + 16);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.t_empty[ai]);
-        const float score = head_reduce_finish(part);
+        const float score = head_reduce_finish<kAbsAdd>(part);
         float kscale = 1.0f;  // MXFP4: the scales are inside the MMA
         if (!kFp4) {
           if (!warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&sm.s_empty[si]);
         }
         const int pos = t * kTileM + p;
-        float v = pos < rlen ? score * kscale : -__int_as_float(0x7f800000);
+        float v = (kIn || pos < rlen) ? score * kscale : -__int_as_float(0x7f800000);
         if (kLocal) {
           // a context shard's blocks of 1 << shift positions, no +inf pin (the
           // merge across shards pins the global newest block)
@@ -479,11 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-          if ((lane & 7) == 0 && pos < rlen)
+          if (kIn) {
+            if ((lane & 7) == 0) kp_row[t * (kTileM / kBlock)] = v;
+          } else if ((lane & 7) == 0 && pos < rlen) {
             kp_row[t * (kTileM / kBlock)] = (pos >> 3) == nb - 1 ? __int_as_float(0x7f800000) : v;
+          }
         }
         return true;
       };
+      using kYes = std::true_type;
+      using kNo = std::false_type;
       const int end = off + take;
       if (R == 3) {
         // two accumulator stages: tiles in pairs, stage 0 then stage 1, so
@@ -491,19 +503,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t = off;
         bool ok = true;
         if ((ts0 & 1) && t < end) {
-          ok = tile(t, ts0, 1);
+          ok = tile(t, ts0, 1, kNo{});
           ++t;
         }
         for (; ok && t + 1 < end; t += 2) {
           const uint32_t ts = ts0 + (t - off);
-          ok = tile(t, ts, 0) && tile(t + 1, ts + 1, 1);
+          if ((t + 2) * kTileM < rlen)  // both tiles interior
+            ok = tile(t, ts, 0, kYes{}) && tile(t + 1, ts + 1, 1, kYes{});
+          else
+            ok = tile(t, ts, 0, kNo{}) && tile(t + 1, ts + 1, 1, kNo{});
         }
-        if (ok && t < end) ok = tile(t, ts0 + (t - off), 0);
+        if (ok && t < end) ok = tile(t, ts0 + (t - off), 0, kNo{});
       } else {
         for (int t = off; t < end; ++t) {
           const uint32_t ts = ts0 + (t - off);
           if (static_cast<int>(ts % 3) != epi) continue;  // round-robin warpgroups
-          if (!tile(t, ts, ts & (kNumAcc - 1))) break;
+          if (!tile(t, ts, ts & (kNumAcc - 1), kNo{})) break;
         }
       }
     }

@@ -504,6 +504,7 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
 template <int KV, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a) {
   constexpr bool kFp4 = KV == kKvMxfp4;
+  constexpr bool kAbsAdd = scorer_relu_abs_add<KV>();  // ReLU form: identical to the dense scorer's
   constexpr int kBlockBytes = kBlock * row_bytes<KV>();  // one candidate block's values: 1 KB or 512 B
   constexpr int kPVB = page_value_bytes<KV>(), kPB = page_bytes<KV>();
   extern __shared__ uint8_t smem_raw[];
@@ -769,14 +770,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
           const uint32_t taddr = tmem_addr(tbase, 32 * quad, ar.idx * kHeads);
           tmem_ld32(taddr, x);
           tmem_ld_wait();
-          head_reduce_half(acc, x, w2);
+          head_reduce_half<kAbsAdd>(acc, x, w2);
           tmem_ld32(taddr + 32, x);
           tmem_ld_wait();
-          head_reduce_half(acc, x, w2 + 16);
+          head_reduce_half<kAbsAdd>(acc, x, w2 + 16);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.t_empty[ar.idx]);
-          const float score = head_reduce_finish(acc);
+          const float score = head_reduce_finish<kAbsAdd>(acc);
           tmem_st1(score_col + t, valid ? order_key(score * kscale) : 0u);
           nvalid_seen += __popc(__ballot_sync(0xffffffffu, valid));
         }
