@@ -22,11 +22,15 @@
 //               accumulator stages -- or, for MXFP4 K, a tcgen05.cp of the
 //               tile's K scale factors and two kind::mxf4 steps of K = 64;
 //   warps 1-3   gather a tile's 16 candidate blocks (each contiguous K in its
-//               page: 1 KB FP8, 512 B MXFP4) into a swizzled MMA tile of a
-//               9-deep ring with 16-byte cp.async from every lane (warp g
-//               takes blocks g, g + 3, ...), each lane arriving on the tile's
-//               barrier once its copies have landed; for MXFP4 they also stage
-//               the 128 positions' scale words for the MMA warp's tcgen05.cp;
+//               page) into a swizzled MMA tile of a 9-deep ring.  FP8 (1 KB
+//               blocks): tiles go round-robin to the three warps, and lanes
+//               0-15 of the tile's warp each issue one tensor-map load of an
+//               8-row box (128-byte swizzle) in a single instruction, the
+//               tile's barrier counting the bytes.  MXFP4 (512 B blocks):
+//               16-byte cp.async from every lane of all three warps (warp g
+//               takes blocks g, g + 3, ...), each lane arriving once its
+//               copies have landed, plus the 128 positions' scale words staged
+//               for the MMA warp's tcgen05.cp;
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
 //               then, two rows ahead, the page of every candidate block, the
 //               query (widened from e2m1 to e4m3 against FP8 K, packed against
@@ -501,8 +505,23 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   }
 }
 
+// The layers' tensor maps over their pools (8-row boxes, one candidate block).
+struct SelectMaps {
+  CUtensorMap m[kMaxSelectLayers];
+};
+// A tensor-map load issued by every active lane (each lane its own box).
+__device__ __forceinline__ void tma_load_3d_lane(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                 uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 template <int KV, bool kMulti>
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    select_kernel(const __grid_constant__ SelectMaps maps, const SelectArgs a) {
   constexpr bool kFp4 = KV == kKvMxfp4;
   constexpr bool kAbsAdd = scorer_relu_abs_add<KV>();  // ReLU form: identical to the dense scorer's
   constexpr int kBlockBytes = kBlock * row_bytes<KV>();  // one candidate block's values: 1 KB or 512 B
@@ -518,7 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
   }
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], 32 * kGatherWarps);  // every gather lane, once its copies of the tile landed
+      // FP8: the tile's tensor-map loads (one expect_tx arrival); MXFP4: every
+      // gather lane, once its copies of the tile landed
+      mbar_init(&sm.k_full[s], kFp4 ? 32 * kGatherWarps : 1);
       mbar_init(&sm.k_empty[s], 1);
     }
     for (int s = 0; s < kNumAcc; ++s) {
@@ -580,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
           ok = false;
           break;
         }
-        fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
+        if (kFp4) fence_proxy_async_smem();  // MXFP4 tiles are written through the generic proxy (cp.async)
         tc_fence_after();
         const uint32_t d = tbase + ar.idx * kHeads;
         const uint32_t a0 = smem_u32(sm.kv[kr.idx]);
@@ -608,25 +629,49 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
     // ------------------------------------------------------------------ gather
-    // Every lane copies 16-byte chunks with cp.async (random 1 KB blocks from
-    // L2 or HBM: issued from all lanes, these reach several times the rate of
-    // one lane's tensor-map or bulk copies).  Warp gw takes blocks gw, gw + 3,
-    // ... of each tile; block blk is contiguous in its page and lands on its
-    // own 8-row swizzle atom.  Each lane then arrives on the tile's k_full as
-    // soon as its copies have landed (cp.async.mbarrier.arrive.noinc).
+    // Random 1 KB blocks from L2 or HBM: copies issued by many lanes at once
+    // reach several times the rate of one lane issuing them in turn, and one
+    // tensor-map load per block (a lane each) costs a single instruction per
+    // tile where 16-byte cp.async from every lane costs two per block plus an
+    // arrival per lane.  Block blk is contiguous in its page and lands on its
+    // own 8-row swizzle atom.
     const int gw = warp - kGatherWarp0;
-    const uint32_t dst0 = sw128_offset(lane >> 3, (lane & 7) * 16), dst1 = sw128_offset(4 + (lane >> 3), (lane & 7) * 16);
     Ring kr;  // slot of the next tile to issue
     int ri = 0;
     bool ok = true;
+    uint32_t nt = 0;           // tiles so far (all warps): FP8 tile n is issued by warp n % 3
+    uint32_t last_issued = 0;  // FP8: 1 + sequence number of this warp's last issued tile
+    if (!kFp4 && lane < a.num_layers) prefetch_tmap(&maps.m[lane]);
     for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
       const uint8_t* k_pool = layer_of<kMulti>(a, r.layer).k_pool;
       pin<kMulti>(k_pool);
+      const CUtensorMap* tmap = &maps.m[kMulti ? r.layer : 0];
       ok = warp_wait_lane0(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
-      for (int t = 0; t < r.ntiles && ok; ++t) {
+      for (int t = 0; t < r.ntiles && ok; ++t, ++nt) {
+        if (!kFp4) {
+          // the tile's 16 blocks: one 8-row box each (landing swizzled on its
+          // own atom), issued by lanes 0-15 at once
+          if (nt % kGatherWarps == static_cast<uint32_t>(gw)) {
+            if (!warp_wait_lane0(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int row_base = t * kBlocksPerTile;
+            const int v = lane < kBlocksPerTile && row_base + lane < r.nv ? info[row_base + lane] : -1;
+            const uint32_t live = __ballot_sync(0xffffffffu, v >= 0);
+            if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[kr.idx], __popc(live) * kBlockBytes);
+            __syncwarp();
+            if (v >= 0)
+              tma_load_3d_lane(sm.kv[kr.idx] + lane * kBlockBytes, tmap, 0, ((v >> 7) & 7) * kBlock, v >> 10,
+                               &sm.k_full[kr.idx]);
+            last_issued = nt + 1;
+          }
+          kr.next(kStages);
+          continue;
+        }
         if (!warp_wait_lane0(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -638,27 +683,18 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
         for (int blk = gw; blk < kBlocksPerTile; blk += kGatherWarps) {
           const int v = __shfl_sync(0xffffffffu, my, blk);
           if (v >= 0) {
-            // FP8 (1 KB): lane l copies 16-byte chunks l and l + 32 (rows
-            // l / 8 and 4 + l / 8); MXFP4 (512 B): lane l copies chunk l (row l / 4)
             const uint8_t* src =
                 k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
-            if (kFp4) {
-              cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
-            } else {
-              cp_async16(dst + blk * kBlockBytes + dst0, src);
-              cp_async16(dst + blk * kBlockBytes + dst1, src + 512);
-            }
+            cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
           }
         }
-        if (kFp4) {
-          // the scale words of all 128 positions, staged for tcgen05.cp:
-          // position p = 32 c + l goes to byte 16 l + 4 c
-          for (int p = gw * 32 + lane; p < kTileM; p += 32 * kGatherWarps) {
-            const int v = __shfl_sync(0xffffffffu, my, p >> 3);
-            if (v >= 0)
-              cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
-                        k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
-          }
+        // the scale words of all 128 positions, staged for tcgen05.cp:
+        // position p = 32 c + l goes to byte 16 l + 4 c
+        for (int p = gw * 32 + lane; p < kTileM; p += 32 * kGatherWarps) {
+          const int v = __shfl_sync(0xffffffffu, my, p >> 3);
+          if (v >= 0)
+            cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
+                      k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
         }
         cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         kr.next(kStages);
@@ -667,6 +703,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
       if (ok) mbar_arrive(&sm.info_empty[b]);
     }
     cp_async_wait<0>();
+    if (!kFp4 && !ok && lane == 0) {
+      // no tensor-map load of this warp may still be writing when the CTA exits
+      for (uint32_t i = last_issued > kStages ? last_issued - kStages : 0; i < last_issued; ++i)
+        if (i % kGatherWarps == static_cast<uint32_t>(gw))
+          mbar_wait(&sm.k_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
+    }
     if (!ok && lane == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kTopkWarp0 && warp < kTopkWarp0 + 4) {
     // ------------------------------------------------------------------ top-k of finished rows + next-row prep
@@ -820,7 +862,13 @@ cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t units = static_cast<int64_t>(a.num_layers) * a.p.rows;
   const int grid = units < device_sm_count() ? static_cast<int>(units) : device_sm_count();
-  select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(a);
+  SelectMaps maps;
+  if (KV == kKvFp8)
+    for (int l = 0; l < a.num_layers; ++l) {
+      e = make_pool_tmap(&maps.m[l], a.layer[l].k_pool, a.p.num_pages, KV, kBlock);
+      if (e != cudaSuccess) return e;
+    }
+  select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
