@@ -22,15 +22,13 @@
 //               accumulator stages -- or, for MXFP4 K, a tcgen05.cp of the
 //               tile's K scale factors and two kind::mxf4 steps of K = 64;
 //   warps 1-3   gather a tile's 16 candidate blocks (each contiguous K in its
-//               page) into a swizzled MMA tile of a 9-deep ring.  FP8 (1 KB
-//               blocks): tiles go round-robin to the three warps, and lanes
-//               0-15 of the tile's warp each issue one tensor-map load of an
-//               8-row box (128-byte swizzle) in a single instruction, the
-//               tile's barrier counting the bytes.  MXFP4 (512 B blocks):
-//               16-byte cp.async from every lane of all three warps (warp g
-//               takes blocks g, g + 3, ...), each lane arriving once its
-//               copies have landed, plus the 128 positions' scale words staged
-//               for the MMA warp's tcgen05.cp;
+//               page: 1 KB FP8, 512 B MXFP4) into a swizzled MMA tile of a
+//               9-deep ring: tiles go round-robin to the three warps, and
+//               lanes 0-15 of the tile's warp each issue one tensor-map load
+//               of an 8-row box (128- or 64-byte swizzle) in a single
+//               instruction, the tile's barrier counting the bytes; for MXFP4
+//               the same warp stages the 128 positions' scale words for the
+//               MMA warp's tcgen05.cp with 4-byte cp.async;
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
 //               then, two rows ahead, the page of every candidate block, the
 //               query (widened from e2m1 to e4m3 against FP8 K, packed against
@@ -537,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
-      // FP8: the tile's tensor-map loads (one expect_tx arrival); MXFP4: every
-      // gather lane, once its copies of the tile landed
-      mbar_init(&sm.k_full[s], kFp4 ? 32 * kGatherWarps : 1);
+      // the tile's tensor-map loads (one expect_tx arrival), and for MXFP4
+      // every lane of the issuing warp once its scale-word copies landed
+      mbar_init(&sm.k_full[s], kFp4 ? 1 + 32 : 1);
       mbar_init(&sm.k_empty[s], 1);
     }
     for (int s = 0; s < kNumAcc; ++s) {
@@ -641,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t nt = 0;           // tiles so far (all warps): FP8 tile n is issued by warp n % 3
     uint32_t last_issued = 0;  // FP8: 1 + sequence number of this warp's last issued tile
-    if (!kFp4 && lane < a.num_layers) prefetch_tmap(&maps.m[lane]);
+    if (lane < a.num_layers) prefetch_tmap(&maps.m[lane]);
     for (int u = unit_of<kMulti>(ri); u < rows && ok; u = unit_of<kMulti>(++ri)) {
       const RowInfo r = row_info<kMulti>(a, u, false);
       const int b = ri & 1;
@@ -651,59 +649,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait_lane0(&sm.info_full[b], (ri >> 1) & 1, abort_flag);
       const int32_t* info = sm.info[b];
       for (int t = 0; t < r.ntiles && ok; ++t, ++nt) {
-        if (!kFp4) {
-          // the tile's 16 blocks: one 8-row box each (landing swizzled on its
-          // own atom), issued by lanes 0-15 at once
-          if (nt % kGatherWarps == static_cast<uint32_t>(gw)) {
-            if (!warp_wait_lane0(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const int row_base = t * kBlocksPerTile;
-            const int v = lane < kBlocksPerTile && row_base + lane < r.nv ? info[row_base + lane] : -1;
-            const uint32_t live = __ballot_sync(0xffffffffu, v >= 0);
-            if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[kr.idx], __popc(live) * kBlockBytes);
-            __syncwarp();
-            if (v >= 0)
-              tma_load_3d_lane(sm.kv[kr.idx] + lane * kBlockBytes, tmap, 0, ((v >> 7) & 7) * kBlock, v >> 10,
-                               &sm.k_full[kr.idx]);
-            last_issued = nt + 1;
+        // the tile's 16 blocks: one 8-row box each (landing swizzled on its
+        // own atom), issued by lanes 0-15 at once
+        if (nt % kGatherWarps == static_cast<uint32_t>(gw)) {
+          if (!warp_wait_lane0(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
           }
-          kr.next(kStages);
-          continue;
-        }
-        if (!warp_wait_lane0(&sm.k_empty[kr.idx], kr.phase ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* dst = sm.kv[kr.idx];
-        const int row_base = t * kBlocksPerTile;
-        const int my = lane < kBlocksPerTile && row_base + lane < r.nv ? info[row_base + lane] : -1;
-#pragma unroll
-        for (int blk = gw; blk < kBlocksPerTile; blk += kGatherWarps) {
-          const int v = __shfl_sync(0xffffffffu, my, blk);
-          if (v >= 0) {
-            const uint8_t* src =
-                k_pool + static_cast<int64_t>(v >> 10) * kPB + ((v >> 7) & 7) * kBlockBytes + lane * 16;
-            cp_async16(dst + blk * kBlockBytes + sw64_offset(lane >> 2, (lane & 3) * 16), src);
-          }
-        }
-        // the scale words of all 128 positions, staged for tcgen05.cp:
-        // position p = 32 c + l goes to byte 16 l + 4 c
-        for (int p = gw * 32 + lane; p < kTileM; p += 32 * kGatherWarps) {
-          const int v = __shfl_sync(0xffffffffu, my, p >> 3);
+          uint8_t* dst = sm.kv[kr.idx];
+          const int row_base = t * kBlocksPerTile;
+          const int v = lane < kBlocksPerTile && row_base + lane < r.nv ? info[row_base + lane] : -1;
+          const uint32_t live = __ballot_sync(0xffffffffu, v >= 0);
+          if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[kr.idx], __popc(live) * kBlockBytes);
+          __syncwarp();
           if (v >= 0)
-            cp_async4(dst + 8192 + 16 * (p & 31) + 4 * (p >> 5),
-                      k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
+            tma_load_3d_lane(dst + lane * kBlockBytes, tmap, 0, ((v >> 7) & 7) * kBlock, v >> 10, &sm.k_full[kr.idx]);
+          if (kFp4) {
+            // the scale words of all 128 positions, staged for tcgen05.cp:
+            // position p = 32 c + l goes to byte 16 l + 4 c; every lane
+            // arrives once its four copies have landed
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int p = 32 * c + lane;
+              const int vb = __shfl_sync(0xffffffffu, v, p >> 3);
+              if (vb >= 0)
+                cp_async4(dst + 8192 + 16 * lane + 4 * c,
+                          k_pool + static_cast<int64_t>(vb >> 10) * kPB + kPVB + 4 * (((vb >> 7) & 7) * kBlock + (p & 7)));
+            }
+            cp_async_arrive_noinc(&sm.k_full[kr.idx]);
+          }
+          last_issued = nt + 1;
         }
-        cp_async_arrive_noinc(&sm.k_full[kr.idx]);
         kr.next(kStages);
       }
       __syncwarp();
       if (ok) mbar_arrive(&sm.info_empty[b]);
     }
     cp_async_wait<0>();
-    if (!kFp4 && !ok && lane == 0) {
+    if (!ok && lane == 0) {
       // no tensor-map load of this warp may still be writing when the CTA exits
       for (uint32_t i = last_issued > kStages ? last_issued - kStages : 0; i < last_issued; ++i)
         if (i % kGatherWarps == static_cast<uint32_t>(gw))
@@ -863,11 +846,10 @@ cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
   const int64_t units = static_cast<int64_t>(a.num_layers) * a.p.rows;
   const int grid = units < device_sm_count() ? static_cast<int>(units) : device_sm_count();
   SelectMaps maps;
-  if (KV == kKvFp8)
-    for (int l = 0; l < a.num_layers; ++l) {
-      e = make_pool_tmap(&maps.m[l], a.layer[l].k_pool, a.p.num_pages, KV, kBlock);
-      if (e != cudaSuccess) return e;
-    }
+  for (int l = 0; l < a.num_layers; ++l) {
+    e = make_pool_tmap(&maps.m[l], a.layer[l].k_pool, a.p.num_pages, KV, kBlock);
+    if (e != cudaSuccess) return e;
+  }
   select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
