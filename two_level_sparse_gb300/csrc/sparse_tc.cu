@@ -593,34 +593,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         bdesc[k] = kFp4 ? sdesc_k64_sw64(smem_u32(sm.q[b]) + 32 * (k & 1)) : sdesc_k128_sw128(smem_u32(sm.q[b]) + 32 * k);
         idesc[k] = kFp4 ? idesc_mxf4(kTileM, kHeads, 2 * (k & 1), 2 * (k & 1)) : idesc_mxf8f6f4_e4m3(kTileM, kHeads, k, k);
       }
-      for (int t = 0; t < r.ntiles; ++t) {
-        if (!warp_wait_lane0(&sm.k_full[kr.idx], kr.phase, abort_flag) ||
-            !warp_wait_lane0(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag)) {
+      // One tile: its MMAs into accumulator stage acc, then the commits that
+      // free the K slot and hand the stage to the scoring warps.
+      auto issue = [&](const Ring& k, const Ring& acc) {
+        const uint32_t d = tbase + acc.idx * kHeads;
+        const uint32_t a0 = smem_u32(sm.kv[k.idx]);
+        if (kFp4) {
+          // the tile's A scale factors (staged transposed by the gather warp),
+          // one slot per accumulator stage: the MMAs that read a slot finished
+          // before t_empty let this stage be reused
+          const uint32_t sfa = tbase + kSfa4Col + 4 * acc.idx;
+          tmem_cp_32x128b_x4_elect(sfa, sdesc_rows16(a0 + 8192));
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_mxf4_elect(d, sdesc_k64_sw64(a0 + 32 * kk), bdesc[kk], idesc[kk], sfa, sfb, kk);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol, sfb, kk);
+        }
+        mma_commit_elect(&sm.k_empty[k.idx]);
+        mma_commit_elect(&sm.t_full[acc.idx]);
+      };
+      // Two tiles per pass where the row has them: lane 0 probes all their
+      // barriers before acting on any probe, so the probes' latencies overlap
+      // (this warp's loop sets the pace of the whole pipeline), and falls back
+      // to bounded waits only when a probe finds a phase incomplete.
+      for (int t = 0; t < r.ntiles; t += 2) {
+        const bool two = t + 1 < r.ntiles;
+        Ring k2 = kr, a2 = ar;
+        k2.next(kStages);
+        a2.next(kNumAcc);
+        bool ready = true;
+        if (lane == 0) {
+          bool p0 = mbar_try_wait(&sm.k_full[kr.idx], kr.phase);
+          bool p1 = mbar_try_wait(&sm.t_empty[ar.idx], ar.phase ^ 1);
+          bool p2 = true, p3 = true;
+          if (two) {
+            p2 = mbar_try_wait(&sm.k_full[k2.idx], k2.phase);
+            p3 = mbar_try_wait(&sm.t_empty[a2.idx], a2.phase ^ 1);
+          }
+          if (!(p0 && p1 && p2 && p3))
+            ready = mbar_wait(&sm.k_full[kr.idx], kr.phase, abort_flag) &&
+                    mbar_wait(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag) &&
+                    (!two || (mbar_wait(&sm.k_full[k2.idx], k2.phase, abort_flag) &&
+                              mbar_wait(&sm.t_empty[a2.idx], a2.phase ^ 1, abort_flag)));
+        }
+        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        __syncwarp();
+        if (!ready) {
           ok = false;
           break;
         }
-        if (kFp4) fence_proxy_async_smem();  // MXFP4 tiles are written through the generic proxy (cp.async)
+        if (kFp4) fence_proxy_async_smem();  // MXFP4 scale words are written through the generic proxy (cp.async)
         tc_fence_after();
-        const uint32_t d = tbase + ar.idx * kHeads;
-        const uint32_t a0 = smem_u32(sm.kv[kr.idx]);
-        if (kFp4) {
-          // the tile's A scale factors (staged transposed by the gather warps),
-          // one slot per accumulator stage: the MMAs that read a slot finished
-          // before t_empty let this stage be reused
-          const uint32_t sfa = tbase + kSfa4Col + 4 * ar.idx;
-          tmem_cp_32x128b_x4_elect(sfa, sdesc_rows16(a0 + 8192));
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            mma_mxf4_elect(d, sdesc_k64_sw64(a0 + 32 * k), bdesc[k], idesc[k], sfa, sfb, k);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * k), bdesc[k], idesc[k], tbase + kSfaCol, sfb, k);
+        issue(kr, ar);
+        if (two) issue(k2, a2);
+        kr = k2;
+        ar = a2;
+        if (two) {
+          kr.next(kStages);
+          ar.next(kNumAcc);
         }
-        mma_commit_elect(&sm.k_empty[kr.idx]);
-        mma_commit_elect(&sm.t_full[ar.idx]);
-        kr.next(kStages);
-        ar.next(kNumAcc);
       }
       if (ok) mma_commit_elect(&sm.q_empty[b]);  // the query buffer is free once these MMAs complete
     }
