@@ -617,38 +617,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Two tiles per pass where the row has them: lane 0 probes all their
       // barriers before acting on any probe, so the probes' latencies overlap
-      // (this warp's loop sets the pace of the whole pipeline), and falls back
-      // to bounded waits only when a probe finds a phase incomplete.
+      // (this warp's loop sets the pace of the whole pipeline); the first
+      // tile goes as soon as its own two have passed, and bounded waits run
+      // only where a probe found a phase incomplete.
+      auto go = [&](bool probed, const Ring& k, const Ring& acc) -> bool {
+        bool ready = true;
+        if (lane == 0 && !probed)
+          ready = mbar_wait(&sm.k_full[k.idx], k.phase, abort_flag) &&
+                  mbar_wait(&sm.t_empty[acc.idx], acc.phase ^ 1, abort_flag);
+        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        __syncwarp();
+        if (!ready) return false;
+        if (kFp4) fence_proxy_async_smem();  // MXFP4 scale words are written through the generic proxy (cp.async)
+        tc_fence_after();
+        issue(k, acc);
+        return true;
+      };
       for (int t = 0; t < r.ntiles; t += 2) {
         const bool two = t + 1 < r.ntiles;
         Ring k2 = kr, a2 = ar;
         k2.next(kStages);
         a2.next(kNumAcc);
-        bool ready = true;
+        bool pa = true, pb = true;  // lane 0: both barriers of tile a / b seen complete
         if (lane == 0) {
-          bool p0 = mbar_try_wait(&sm.k_full[kr.idx], kr.phase);
-          bool p1 = mbar_try_wait(&sm.t_empty[ar.idx], ar.phase ^ 1);
+          const bool p0 = mbar_try_wait(&sm.k_full[kr.idx], kr.phase);
+          const bool p1 = mbar_try_wait(&sm.t_empty[ar.idx], ar.phase ^ 1);
           bool p2 = true, p3 = true;
           if (two) {
             p2 = mbar_try_wait(&sm.k_full[k2.idx], k2.phase);
             p3 = mbar_try_wait(&sm.t_empty[a2.idx], a2.phase ^ 1);
           }
-          if (!(p0 && p1 && p2 && p3))
-            ready = mbar_wait(&sm.k_full[kr.idx], kr.phase, abort_flag) &&
-                    mbar_wait(&sm.t_empty[ar.idx], ar.phase ^ 1, abort_flag) &&
-                    (!two || (mbar_wait(&sm.k_full[k2.idx], k2.phase, abort_flag) &&
-                              mbar_wait(&sm.t_empty[a2.idx], a2.phase ^ 1, abort_flag)));
+          pa = p0 && p1;
+          pb = p2 && p3;
         }
-        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-        __syncwarp();
-        if (!ready) {
+        if (!go(pa, kr, ar) || (two && !go(pb, k2, a2))) {
           ok = false;
           break;
         }
-        if (kFp4) fence_proxy_async_smem();  // MXFP4 scale words are written through the generic proxy (cp.async)
-        tc_fence_after();
-        issue(kr, ar);
-        if (two) issue(k2, a2);
         kr = k2;
         ar = a2;
         if (two) {
