@@ -254,6 +254,49 @@ __device__ __forceinline__ void mma_mxf4_elect(uint32_t d_tmem, uint64_t adesc, 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// One 128-position tile of the select: four kind::mxf8f6f4 steps of K = 32
+// (A descriptors a0 + 2 k: 32 bytes further along each K-major row; the first
+// step overwrites the accumulator), then commits arriving on bar0 and bar1 --
+// all issued by one elected lane.
+__device__ __forceinline__ void mma_tile_mxf8f6f4_commit2_elect(uint32_t d_tmem, uint64_t a0, const uint64_t (&b)[4],
+                                                                const uint32_t (&i)[4], uint32_t sfa_tmem,
+                                                                uint32_t sfb_tmem, uint32_t bar0, uint32_t bar1) {
+  asm volatile(
+      "{\n\t.reg .pred e, z, o;\n\t.reg .b64 a1, a2, a3;\n\t"
+      "setp.ne.b32 z, %0, %0;\n\tsetp.eq.b32 o, %0, %0;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %6, [%10], [%11], z;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a1, %3, %7, [%10], [%11], o;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a2, %4, %8, [%10], [%11], o;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a3, %5, %9, [%10], [%11], o;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%13];\n\t}" ::"r"(d_tmem),
+      "l"(a0), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(i[0]), "r"(i[1]), "r"(i[2]), "r"(i[3]),
+      "r"(sfa_tmem), "r"(sfb_tmem), "r"(bar0), "r"(bar1)
+      : "memory");
+}
+// The MXFP4 counterpart: the tile's A scale factors copied into tensor memory
+// (tcgen05.cp 32x128b.warpx4 from sf_desc), two kind::mxf4 steps of K = 64
+// (A descriptors a0 and a0 + 2), the commits.
+__device__ __forceinline__ void mma_tile_mxf4_commit2_elect(uint32_t d_tmem, uint64_t a0, const uint64_t (&b)[4],
+                                                            const uint32_t (&i)[4], uint64_t sf_desc,
+                                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t bar0,
+                                                            uint32_t bar1) {
+  asm volatile(
+      "{\n\t.reg .pred e, z, o;\n\t.reg .b64 a1;\n\t"
+      "setp.ne.b32 z, %0, %0;\n\tsetp.eq.b32 o, %0, %0;\n\t"
+      "add.s64 a1, %1, 2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %4, [%7], [%8], z;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a1, %3, %5, [%7], [%8], o;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}" ::"r"(d_tmem),
+      "l"(a0), "l"(b[0]), "l"(b[1]), "r"(i[0]), "r"(i[1]), "l"(sf_desc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(bar0),
+      "r"(bar1)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"

@@ -598,22 +598,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue = [&](const Ring& k, const Ring& acc) {
         const uint32_t d = tbase + acc.idx * kHeads;
         const uint32_t a0 = smem_u32(sm.kv[k.idx]);
-        if (kFp4) {
+        const uint32_t ke = smem_u32(&sm.k_empty[k.idx]), tf = smem_u32(&sm.t_full[acc.idx]);
+        if (kFp4)
           // the tile's A scale factors (staged transposed by the gather warp),
           // one slot per accumulator stage: the MMAs that read a slot finished
           // before t_empty let this stage be reused
-          const uint32_t sfa = tbase + kSfa4Col + 4 * acc.idx;
-          tmem_cp_32x128b_x4_elect(sfa, sdesc_rows16(a0 + 8192));
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_mxf4_elect(d, sdesc_k64_sw64(a0 + 32 * kk), bdesc[kk], idesc[kk], sfa, sfb, kk);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_mxf8f6f4_elect(d, sdesc_k128_sw128(a0 + 32 * kk), bdesc[kk], idesc[kk], tbase + kSfaCol, sfb, kk);
-        }
-        mma_commit_elect(&sm.k_empty[k.idx]);
-        mma_commit_elect(&sm.t_full[acc.idx]);
+          mma_tile_mxf4_commit2_elect(d, sdesc_k64_sw64(a0), bdesc, idesc, sdesc_rows16(a0 + 8192),
+                                      tbase + kSfa4Col + 4 * acc.idx, sfb, ke, tf);
+        else
+          mma_tile_mxf8f6f4_commit2_elect(d, sdesc_k128_sw128(a0), bdesc, idesc, tbase + kSfaCol, sfb, ke, tf);
       };
       // Two tiles per pass where the row has them: lane 0 probes all their
       // barriers before acting on any probe, so the probes' latencies overlap
