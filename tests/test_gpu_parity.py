@@ -719,6 +719,34 @@ def test_select_layers_equals_one_launch_per_layer(ci, case):
 
 
 @needs_cuda
+def test_select_pools_beyond_l2_one_launch_per_layer(ci):
+    """The 64-row decode batch, whose pools do not fit in L2 (so the FP8 K
+    scales are fetched tiles ahead): one ci_select_sparse launch per layer
+    writes bit for bit what the step's single all-layer launch wrote (and
+    test_decode_batch_all_rows checks that one against the oracle)."""
+    from two_level_sparse_gb300.step import IndexerStep
+
+    dev = synth.config_workload(1, device="cuda")
+    pool_bytes = dev.layers[0].k_pool.numel()
+    assert pool_bytes > torch.cuda.get_device_properties(0).L2_cache_size // 2
+    step = IndexerStep(dev, with_scores=True)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) == 0
+    for j, layer in enumerate(dev.layers):
+        blocks, nvalid, mb = (step.blocks_src, step.nvalid_src, step.Kp) if j == 0 else (step.blocks, step.nvalid,
+                                                                                        step.K)
+        pos = torch.full_like(step.pos[j], -9)
+        score = torch.full_like(step.score[j], 7.0)
+        ci.ci_select_sparse(layer.q_fp4, layer.q_sf, layer.w, layer.k_pool, dev.page_table, dev.layout, dev.seq_len,
+                            dev.max_len, blocks, nvalid, mb, step.P, pos, score, dev_err=step.dev_err)
+        torch.cuda.synchronize()
+        assert torch.equal(pos, step.pos[j]), j
+        assert torch.equal(score.view(torch.int32), step.score[j].view(torch.int32)), j
+    assert int(step.dev_err.item()) == 0
+
+
+@needs_cuda
 @pytest.mark.parametrize("case", ["decode", "prefill"])
 def test_run_host_moves_the_same_results(ci, case):
     """IndexerStep.run_host (pinned host in, pinned host out, copies overlapped

@@ -21,6 +21,18 @@ int device_sm_count() {
   return counts[dev];
 }
 
+int64_t device_l2_bytes() {
+  static int64_t sizes[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (sizes[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev);
+    sizes[dev] = n > 0 ? n : 1;
+  }
+  return sizes[dev];
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;

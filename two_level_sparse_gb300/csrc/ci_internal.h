@@ -142,6 +142,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 
 // Shared host helpers (ci_api.cu).
 int device_sm_count();
+int64_t device_l2_bytes();  // L2 cache size of the current device
 // Tensor map over the value bytes of a paged index-K pool viewed as
 // [num_pages][64 positions][128 bytes], 128-byte swizzle, box of `box_rows`
 // positions of one page.

@@ -96,6 +96,7 @@ struct __align__(1024) Smem {
   int topk_go;
   int prep_ok[4];
   uint32_t kmin, kmax;
+  float kring[8][3][32];  // FP8 K scales fetched ahead, per scoring warp: 3 tiles x 32 positions
   TopkShared topk;
 };
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
@@ -517,7 +518,8 @@ __device__ __forceinline__ void tma_load_3d_lane(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-template <int KV, bool kMulti>
+// kRing: FP8 K scales fetched tiles ahead (pools too large to stay in L2).
+template <int KV, bool kMulti, bool kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     select_kernel(const __grid_constant__ SelectMaps maps, const SelectArgs a) {
   constexpr bool kFp4 = KV == kKvMxfp4;
@@ -805,18 +807,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t score_col = tmem_addr(tbase, 32 * quad, kScoreCol + b * kMaxTiles);
       uint32_t nvalid_seen = 0;
+      // FP8 K scales.  From a pool in L2: each lane loads its position's
+      // scale as the tile starts.  From a pool in HBM (kRing): this warp's
+      // tiles alternate with the other warpgroup's, and each lane copies its
+      // position's scale two of the warp's tiles ahead (cp.async, one group
+      // per tile) into a 3-slot ring of its own, so that the load has four
+      // tiles of time to land.  (MXFP4: the scales are inside the MMA.)
+      constexpr bool ks_ring = !kFp4 && kRing;
+      float* kring = &sm.kring[warp - kScoreWarp0][0][0];
+      auto ks_issue = [&](int tt, int slot) {
+        if (!ks_ring) return;
+        const int s2 = tt * kBlocksPerTile + (p >> 3);
+        const int v = tt < r.ntiles && s2 < r.nv ? sm.info[b][s2] : -1;
+        const int off = (v >> 4) & 7;
+        if (v >= 0 && (p & 7) >= off && (p & 7) < off + (v & 15))
+          cp_async4(kring + 32 * slot + lane,
+                    k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB + 4 * (((v >> 7) & 7) * kBlock + (p & 7)));
+        cp_async_commit();
+      };
+      const int t_first = static_cast<int>((static_cast<uint32_t>(e) - tseq) & 1u);  // this warp's first tile
+      int own = 0;  // this warp's tiles of the row so far
+      ks_issue(t_first, 0);
+      ks_issue(t_first + 2, 1);
       for (int t = 0; t < r.ntiles; ++t, ++tseq) {
         if ((tseq & 1) == static_cast<uint32_t>(e)) {
           const int slot = t * kBlocksPerTile + (p >> 3);
           const int v = slot < r.nv ? sm.info[b][slot] : -1;
           const int off = (v >> 4) & 7;
           const bool valid = v >= 0 && (p & 7) >= off && (p & 7) < off + (v & 15);
-          // this position's K scale, fetched now and used after the head sum
-          // (MXFP4: 1, the scales are inside the MMA)
+          ks_issue(t + 4, (own + 2) % 3);
           float kscale = 1.0f;
-          if (!kFp4 && valid)
+          if (ks_ring) {
+            cp_async_wait<2>();  // this tile's group (the two newest may still be in flight)
+            if (valid) kscale = kring[32 * (own % 3) + lane];
+          } else if (!kFp4 && valid) {
             kscale = __ldg(reinterpret_cast<const float*>(k_pool + static_cast<int64_t>(v >> 10) * kPB + kPVB) +
                            ((v >> 7) & 7) * kBlock + (p & 7));
+          }
+          ++own;
           if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
             ok = false;
             break;
@@ -870,10 +898,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t select_smem_bytes(int) { return sizeof(Smem) + 1024; }
 
-template <int KV, bool kMulti>
+template <int KV, bool kMulti, bool kRing>
 cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
   const int smem = static_cast<int>(select_smem_bytes(0));
-  cudaError_t e = cudaFuncSetAttribute(select_kernel<KV, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel<KV, kMulti, kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t units = static_cast<int64_t>(a.num_layers) * a.p.rows;
   const int grid = units < device_sm_count() ? static_cast<int>(units) : device_sm_count();
@@ -882,8 +910,17 @@ cudaError_t launch_select_kv(const SelectArgs& a, cudaStream_t stream) {
     e = make_pool_tmap(&maps.m[l], a.layer[l].k_pool, a.p.num_pages, KV, kBlock);
     if (e != cudaSuccess) return e;
   }
-  select_kernel<KV, kMulti><<<grid, kThreads, smem, stream>>>(maps, a);
+  select_kernel<KV, kMulti, kRing><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
+}
+
+// FP8 pools: scales fetched ahead when a layer's pool (the layers run one
+// after another) cannot stay in L2.
+template <bool kMulti>
+cudaError_t launch_select_fmt(const SelectArgs& a, cudaStream_t stream) {
+  if (a.p.kv_format == kKvMxfp4) return launch_select_kv<kKvMxfp4, kMulti, false>(a, stream);
+  const bool ring = a.p.num_pages * static_cast<int64_t>(page_bytes<kKvFp8>()) > device_l2_bytes() / 2;
+  return ring ? launch_select_kv<kKvFp8, kMulti, true>(a, stream) : launch_select_kv<kKvFp8, kMulti, false>(a, stream);
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
@@ -897,11 +934,9 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
         s.layer[j] = s.layer[j - 1];
         s.layer[j - 1] = t;
       }
-    return s.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, true>(s, stream)
-                                     : launch_select_kv<kKvFp8, true>(s, stream);
+    return launch_select_fmt<true>(s, stream);
   }
-  return a.p.kv_format == kKvMxfp4 ? launch_select_kv<kKvMxfp4, false>(a, stream)
-                                   : launch_select_kv<kKvFp8, false>(a, stream);
+  return launch_select_fmt<false>(a, stream);
 }
 
 }  // namespace ci
