@@ -211,12 +211,13 @@ def subset_workload(wl_dev, rows):
 
 
 @needs_cuda
+@pytest.mark.parametrize("rows", [40, 400])
 @pytest.mark.parametrize("K1,K2", [(2048, 513), (128, 513), (513, 64)])
-def test_publish_pair_equals_two_single_publishes(ci, K1, K2):
+def test_publish_pair_equals_two_single_publishes(ci, K1, K2, rows):
     """ci_publish_blocks2 returns exactly the two single selections, which
-    equal the oracle's block selection (ties toward the lower block id)."""
-    g = torch.Generator().manual_seed(7)
-    rows = 40
+    equal the oracle's block selection (ties toward the lower block id), on
+    few rows (one per CTA) and on many (four per SM)."""
+    g = torch.Generator().manual_seed(7 + rows)
     lens = torch.randint(1, 40000, (rows,), generator=g, dtype=torch.int32)
     lens[:4] = torch.tensor([1, 8 * K1, 8 * K2 + 3, 8 * max(K1, K2) + 1], dtype=torch.int32)
     max_len = int(lens.max())
@@ -277,17 +278,18 @@ def _publish_rows_against_oracle(ci, keys, lens, K1, K2):
 
 
 @needs_cuda
+@pytest.mark.parametrize("rows", [24, 320])
 @pytest.mark.parametrize("case", ["normal", "ties", "sample_adversarial", "mid_length", "wider_second"])
-def test_publish_long_rows_match_the_oracle(ci, case):
+def test_publish_long_rows_match_the_oracle(ci, case, rows):
     """Rows of thousands of blocks, whose threshold the publish kernel brackets
     from a strided sample of the keys (with the radix path behind it when the
     sample's bound misses): the oracle's selection, ties toward the lower id,
     in every case -- random keys, keys with heavy ties at the threshold, keys
     whose every sampled position (each 16th block) outranks all the others so
     that the sample's bound fails, rows of 4096 - 8192 blocks, and a second
-    selection wider than the first."""
-    g = torch.Generator().manual_seed(91)
-    rows = 24
+    selection wider than the first.  24 rows take the one-row-per-CTA kernel,
+    320 rows (two per SM or more) the kernel with four rows per SM."""
+    g = torch.Generator().manual_seed(91 + rows)
     L = 262144
     lens = torch.full((rows,), L, dtype=torch.int32)
     lens[1] = L - 5  # a ragged newest block

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libci.so")
 BUILD = os.path.join(ROOT, "_build")
-SOURCES = ["ci_api.cu", "dense_tc.cu", "publish.cu", "sparse_tc.cu", "tail.cu", "qprod.cu", "dcp.cu"]
+SOURCES = ["ci_api.cu", "dense_tc.cu", "publish.cu", "publish_rows.cu", "sparse_tc.cu", "tail.cu", "qprod.cu", "dcp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

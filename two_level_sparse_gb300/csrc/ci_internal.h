@@ -134,6 +134,7 @@ struct DcpTopkArgs {
 };
 
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
+cudaError_t launch_publish_rows(const PublishArgs& a, cudaStream_t stream);  // few rows: one per CTA at a time
 cudaError_t launch_dcp_merge_keys(const DcpKeysArgs& a, cudaStream_t stream);
 cudaError_t launch_dcp_merge_topk(const DcpTopkArgs& a, cudaStream_t stream);
 cudaError_t launch_qprod(const QProdArgs& a, cudaStream_t stream);
