@@ -787,7 +787,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = (warp - kScoreWarp0) >> 2;  // scoring warpgroup 0 / 1
     const int quad = warp & 3;
     const int p = 32 * quad + lane;
-    Ring ar;
     uint32_t tseq = 0;
     int ri = 0;
     unsigned long long w2[32];  // head weights, packed pairs
@@ -829,8 +828,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int own = 0;  // this warp's tiles of the row so far
       ks_issue(t_first, 0);
       ks_issue(t_first + 2, 1);
-      for (int t = 0; t < r.ntiles; ++t, ++tseq) {
-        if ((tseq & 1) == static_cast<uint32_t>(e)) {
+      // this warp's tiles of the row: every other one, from t_first; their
+      // accumulator stages follow the tile sequence (stage q % 3, phase q / 3)
+      const uint32_t q0 = tseq + static_cast<uint32_t>(t_first);
+      uint32_t aidx = q0 % kNumAcc, aph = (q0 / kNumAcc) & 1u;
+      for (int t = t_first; t < r.ntiles; t += 2) {
+        {
           const int slot = t * kBlocksPerTile + (p >> 3);
           const int v = slot < r.nv ? sm.info[b][slot] : -1;
           const int off = (v >> 4) & 7;
@@ -845,14 +848,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                            ((v >> 7) & 7) * kBlock + (p & 7));
           }
           ++own;
-          if (!warp_wait(&sm.t_full[ar.idx], ar.phase, abort_flag)) {
+          if (!warp_wait_fast(&sm.t_full[aidx], aph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           HeadAcc acc = {{0, 0, 0, 0}};
           uint32_t x[32];
-          const uint32_t taddr = tmem_addr(tbase, 32 * quad, ar.idx * kHeads);
+          const uint32_t taddr = tmem_addr(tbase, 32 * quad, aidx * kHeads);
           tmem_ld32(taddr, x);
           tmem_ld_wait();
           head_reduce_half<kAbsAdd>(acc, x, w2);
@@ -861,13 +864,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           head_reduce_half<kAbsAdd>(acc, x, w2 + 16);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.t_empty[ar.idx]);
+          if (lane == 0) mbar_arrive(&sm.t_empty[aidx]);
           const float score = head_reduce_finish<kAbsAdd>(acc);
           tmem_st1(score_col + t, valid ? order_key(score * kscale) : 0u);
           nvalid_seen += __popc(__ballot_sync(0xffffffffu, valid));
         }
-        ar.next(kNumAcc);
+        static_assert(kNumAcc >= 2, "the stage steps by two with one wrap at most");
+        aidx += 2;
+        if (aidx >= kNumAcc) {
+          aidx -= kNumAcc;
+          aph ^= 1u;
+        }
       }
+      tseq += static_cast<uint32_t>(r.ntiles);
       if (!ok) break;
       tmem_st_wait();
       tc_fence_before();
