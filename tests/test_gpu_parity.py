@@ -195,6 +195,24 @@ def test_full_size_config_sampled_rows(ci, cid):
     assert_ok(compare.check_step(sub, sub_out))
 
 
+@needs_cuda
+def test_full_size_prefill_chunk_more_rows(ci):
+    """Sixteen more rows of the 16384-row chunk at 262144 positions, spread
+    over the chunk with every residue mod 3 and mod 4 (the dense pass's
+    three-row groups, the publish kernel's four row groups per CTA, the
+    select's CTAs), against the oracle: keys, both block tables and every
+    layer's top-512."""
+    wl_dev = synth.config_workload(4, device="cuda")
+    step = run_step(None, wl_dev=wl_dev)
+    assert int(step.dev_err.item()) == 0
+    rows = [1021 * i + (i % 3) for i in range(16)]
+    assert len({r % 3 for r in rows}) == 3 and len({r % 4 for r in rows}) == 4
+    sub = subset_workload(wl_dev, rows)
+    out = step.outputs_numpy()
+    sub_out = {k: (v[:, rows] if k in ("pos", "score") else v[rows]) for k, v in out.items()}
+    assert_ok(compare.check_step(sub, sub_out))
+
+
 def subset_workload(wl_dev, rows):
     """The sampled rows' operands on the CPU (the whole pool comes along)."""
     idx = torch.tensor(rows, dtype=torch.long, device=wl_dev.seq_len.device)
