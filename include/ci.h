@@ -115,7 +115,7 @@ enum ci_status {
   CI_ERR_SHAPE = -2,       /* inconsistent sizes or strides */
   CI_ERR_ALIGN = -3,       /* a pointer or stride breaks an alignment rule */
   CI_ERR_RANGE = -4,       /* a size is out of its supported range */
-  CI_ERR_UNSUPPORTED = -5, /* a valid request this build does not implement */
+  CI_ERR_UNSUPPORTED = -5, /* a valid request this library does not implement */
   CI_ERR_CUDA = -6         /* a CUDA call failed (launch or attribute) */
 };
 

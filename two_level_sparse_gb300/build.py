@@ -3,7 +3,7 @@
 Each translation unit is compiled in parallel with nvcc, then linked into one
 shared object with the CUDA runtime linked statically, so the library loads
 on a machine without a GPU driver (its entry points then fail with
-CI_ERR_CUDA).  The tensor-map encoder of the driver is looked up at run time.
+CI_ERR_CUDA).  The CUDA driver's tensor-map encoder is looked up at run time.
 """
 from __future__ import annotations
 

@@ -118,7 +118,7 @@ const char* ci_strerror(int status) {
     case CI_ERR_SHAPE: return "inconsistent sizes or strides";
     case CI_ERR_ALIGN: return "a pointer or stride breaks an alignment rule";
     case CI_ERR_RANGE: return "a size is out of its supported range";
-    case CI_ERR_UNSUPPORTED: return "a valid request this build does not implement";
+    case CI_ERR_UNSUPPORTED: return "a valid request this library does not implement";
     case CI_ERR_CUDA: return "a CUDA call failed";
     default: return "unknown status";
   }
