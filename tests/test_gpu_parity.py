@@ -230,7 +230,7 @@ def subset_workload(wl_dev, rows):
 
 @needs_cuda
 @pytest.mark.parametrize("rows", [40, 400])
-@pytest.mark.parametrize("K1,K2", [(2048, 513), (128, 513), (513, 64)])
+@pytest.mark.parametrize("K1,K2", [(2048, 513), (128, 513), (513, 64), (4096, 1000)])
 def test_publish_pair_equals_two_single_publishes(ci, K1, K2, rows):
     """ci_publish_blocks2 returns exactly the two single selections, which
     equal the oracle's block selection (ties toward the lower block id), on
