@@ -10,15 +10,19 @@
 // variant.)  The [rows, L] score matrix is never written.
 //
 // Design (one persistent CTA per SM, 16 warps):
-//   warp 0      TMA producer: two 64-position pages of FP8 K per 128-position
-//               tile (one tensor-map load each, 128-byte swizzle) into an
-//               8-stage ring, their fp32 scales (bulk copies) into a separate
-//               16-slot ring;
+//   warps 0, 2  TMA producers (warp 0 the even tiles of the sequence, warp 2
+//               the odd ones, so that the producer work sits on two
+//               sub-partitions beside the epilogue warps, not one): two
+//               64-position pages of FP8 K per
+//               128-position tile (one tensor-map load each, 128-byte
+//               swizzle) into an 8-stage ring, their fp32 scales (bulk
+//               copies) into a separate 16-slot ring;
 //   warp 1      MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale, M = 128
 //               positions, N = 64 R columns (R rows x 64 heads), K = 128 in
 //               four K = 32 steps; A = K tile (scale 1), B = the rows' queries
 //               widened from e2m1 to e4m3 (exact) with their ue8m0 scales in
 //               tensor memory; fp32 accumulators in tensor memory;
+//   warp 3      set-up only;
 //   warps 4-15  epilogue, three warpgroups: tcgen05.ld of one row's 64 head
 //               columns per position, ReLU + head weights, K scale, length
 //               mask, max over 8 lanes by shuffles, key store.
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long remaining = sm.t_end - sm.t_begin;
   int g = sm.g_begin, off = sm.o_begin;
   uint32_t tseq = 0;    // tiles so far: every ring slot and phase derives from it
-  uint32_t issued = 0;  // TMA thread: tiles whose loads were issued
+  uint32_t issued = 0;  // producer warps: one past the sequence number of the last tile this warp issued
   const int epi = warp >= kEpiWarp0 ? (warp - kEpiWarp0) >> 2 : -1;  // epilogue warpgroup
   const int quad = warp & 3;
   unsigned long long w2[32];  // head weights, packed pairs
@@ -338,8 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
 
-    if (warp == 0) {
-      // ---------------------------------------------------------------- TMA producer
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------------------- TMA producers
+      // warp 0 the even tiles of the sequence, warp 2 the odd ones, so that
+      // the producer work sits on two sub-partitions, not one
+      const uint32_t par = static_cast<uint32_t>(warp >> 1);
       const int req = grp.req;
       const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
       const int end = off + take;
@@ -352,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c0 + 32 + lane < end) nxt = load_tile_pages(pt, c0 + 32 + lane, glen, a.p.num_pages, a.p.dev_err);
         const int n = min(32, end - c0);
         for (int i = 0; i < n; ++i, ++ts) {
+          if ((ts & 1u) != par) continue;
           const int pid[2] = {__shfl_sync(0xffffffffu, cur.lo, i), __shfl_sync(0xffffffffu, cur.hi, i)};
           const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
           const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load_elect(&sm.ks[si][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPB + kPVB, kPage * 4,
                             &sm.s_full[si]);
           }
-          ++issued;
+          issued = ts + 1;
         }
       }
     } else if (warp == 1) {
@@ -536,8 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0, nullptr, 1000000000ull);
     }
-    if (warp == 0 && lane == 0) {
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // this producer's tiles (its parity) among the last kStages issued
+      const uint32_t par = static_cast<uint32_t>(warp >> 1);
       for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+        if ((i & 1u) != par) continue;
         mbar_wait(&sm.k_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
         mbar_wait(&sm.s_full[i % kScaleSlots], (i / kScaleSlots) & 1, nullptr, 1000000000ull);
       }
