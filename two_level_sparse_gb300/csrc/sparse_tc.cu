@@ -191,7 +191,9 @@ struct Ring {
 // Prep threads, one row ahead: the query widened from e2m1 to e4m3 into the
 // swizzled B tile, its scale factors staged for tcgen05.cp, and for every
 // candidate block its physical page, its slot in the page and how many of its
-// positions lie below L.
+// positions lie below L.  The row's global reads (query, scale words, the
+// first 2048 candidate block ids) are all issued before the first wait, so
+// that their latencies overlap; the page lookups follow as one more batch.
 template <int KV, bool kMulti>
 __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
                                          volatile int* abort_flag) {
@@ -204,43 +206,73 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
   pin<kMulti>(q_fp4);
   pin<kMulti>(q_sf);
   pin<kMulti>(brow);
-  bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
+  // the query's 4 KB: 32 bytes per thread, as four 8-byte words
+  static_assert(kHeads * 64 == kPrepThreads * 32, "four query words per prep thread");
+  uint2 qv[4];
   if (KV == kKvMxfp4) {
-    // packed e2m1 rows of 64 bytes, 64-byte swizzle
-    for (int idx = pid_t; ok && idx < kHeads * 4; idx += kPrepThreads) {
-      const int head = idx >> 2, c = idx & 3;
-      const uint2* src =
-          reinterpret_cast<const uint2*>(q_fp4 + head * 64 + c * 16);
-      const uint2 lo = src[0], hi = src[1];
-      *reinterpret_cast<uint4*>(sm.q[b] + sw64_offset(head, c * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    // thread slots idx = pid_t + 128 j, j < 2: head idx >> 2, 16-byte chunk idx & 3
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int idx = pid_t + kPrepThreads * j;
+      const uint2* src = reinterpret_cast<const uint2*>(q_fp4 + (idx >> 2) * 64 + (idx & 3) * 16);
+      qv[2 * j] = src[0];
+      qv[2 * j + 1] = src[1];
     }
   } else {
-    for (int idx = pid_t; ok && idx < kHeads * 8; idx += kPrepThreads) {
-      const int head = idx >> 3, c = idx & 7;
-      const uint2 packed =
-          *reinterpret_cast<const uint2*>(q_fp4 + head * 64 + c * 8);
-      *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(head, c * 16)) = widen_fp4x16(packed);
+    // thread slots idx = pid_t + 128 j, j < 4: head idx >> 3, 8-byte chunk idx & 7
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = pid_t + kPrepThreads * j;
+      qv[j] = *reinterpret_cast<const uint2*>(q_fp4 + (idx >> 3) * 64 + (idx & 7) * 8);
     }
   }
-  if (ok && pid_t < 32) {
-    // lane l of the scale-factor columns: heads l and 32 + l, byte j = K block j
+  uint32_t sf0 = 0, sf1 = 0;
+  if (pid_t < 32) {
     const uint32_t* sfp = reinterpret_cast<const uint32_t*>(q_sf);
-    *reinterpret_cast<uint4*>(sm.sf[b] + 16 * pid_t) =
-        make_uint4(sfp[pid_t], sfp[32 + pid_t], kUnitScales, kUnitScales);
+    sf0 = sfp[pid_t];
+    sf1 = sfp[32 + pid_t];
+  }
+  constexpr int kBatch = 16;
+  int blk[kBatch];
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    const int i = j * kPrepThreads + pid_t;
+    blk[j] = i < r.nv ? brow[i] : -1;
+  }
+  bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
+  if (ok) {
+    if (KV == kKvMxfp4) {
+      // packed e2m1 rows of 64 bytes, 64-byte swizzle
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int idx = pid_t + kPrepThreads * j;
+        *reinterpret_cast<uint4*>(sm.q[b] + sw64_offset(idx >> 2, (idx & 3) * 16)) =
+            make_uint4(qv[2 * j].x, qv[2 * j].y, qv[2 * j + 1].x, qv[2 * j + 1].y);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int idx = pid_t + kPrepThreads * j;
+        *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(idx >> 3, (idx & 7) * 16)) = widen_fp4x16(qv[j]);
+      }
+    }
+    // lane l of the scale-factor columns: heads l and 32 + l, byte j = K block j
+    if (pid_t < 32) *reinterpret_cast<uint4*>(sm.sf[b] + 16 * pid_t) = make_uint4(sf0, sf1, kUnitScales, kUnitScales);
   }
   fence_proxy_async_smem();
   mbar_arrive(&sm.q_full[b]);
   ok = ok && warp_wait(&sm.info_empty[b], ph ^ 1, abort_flag);  // row ri - 2 gathered and scored
   const int req = row_request(a, r.row);
   const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
-  constexpr int kBatch = 16;
   for (int i0 = 0; ok && i0 < r.nv; i0 += kPrepThreads * kBatch) {
-    int blk[kBatch], pid[kBatch];
+    if (i0 > 0) {
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = i0 + j * kPrepThreads + pid_t;
-      blk[j] = i < r.nv ? brow[i] : -1;
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * kPrepThreads + pid_t;
+        blk[j] = i < r.nv ? brow[i] : -1;
+      }
     }
+    int pid[kBatch];
     // candidate block blk covers positions blk << shift .. + (1 << shift) - 1
     // (8 positions, or a context shard's 4, 2 or 1), inside one 8-position group
     const int sh = a.block_shift;
@@ -454,26 +486,35 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
     }
   }
   named_sync(kTopkBar, kTopkThreads);
-  // Positions, tile-parallel: thread kt walks the selected entries of tiles
-  // kt and kt + 128 (about P / tiles each) in position order.  Rank = entries
-  // above the threshold before it + entries at it before it (capped at
-  // need_eq), in (tile, position) order.
-  for (int t = kt; t < nt; t += kTopkThreads) {
+  // Positions, word-parallel: thread kt walks the selected entries of ballot
+  // words kt, kt + 128, ... (word w of tile t: positions 32 w .. 32 w + 31) in
+  // position order.  Rank = entries above the threshold before it + entries
+  // at it before it (capped at need_eq), in (tile, position) order.
+  for (int it = kt; it < 4 * nt; it += kTopkThreads) {
+    const int t = it >> 2, w = it & 3;
     const uint4 g4 = sm.mgt[t], e4 = sm.meq[t];
-    const uint32_t g[4] = {g4.x, g4.y, g4.z, g4.w}, e[4] = {e4.x, e4.y, e4.z, e4.w};
     uint32_t gtb = static_cast<uint32_t>(sm.gbase[t]), eqb = static_cast<uint32_t>(sm.ebase[t]);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t bits = g[w] | e[w];
-      while (bits) {
-        const int lb = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const uint32_t below = (1u << lb) - 1u;
-        const uint32_t gt_before = gtb + __popc(g[w] & below), eq_before = eqb + __popc(e[w] & below);
-        if (((g[w] >> lb) & 1u) || eq_before < need_eq) emit_pos(static_cast<int>(gt_before + min(eq_before, need_eq)), t, 32 * w + lb);
-      }
-      gtb += __popc(g[w]);
-      eqb += __popc(e[w]);
+    if (w > 0) {
+      gtb += __popc(g4.x);
+      eqb += __popc(e4.x);
+    }
+    if (w > 1) {
+      gtb += __popc(g4.y);
+      eqb += __popc(e4.y);
+    }
+    if (w > 2) {
+      gtb += __popc(g4.z);
+      eqb += __popc(e4.z);
+    }
+    const uint32_t gw = w == 0 ? g4.x : w == 1 ? g4.y : w == 2 ? g4.z : g4.w;
+    const uint32_t ew = w == 0 ? e4.x : w == 1 ? e4.y : w == 2 ? e4.z : e4.w;
+    uint32_t bits = gw | ew;
+    while (bits) {
+      const int lb = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const uint32_t below = (1u << lb) - 1u;
+      const uint32_t gt_before = gtb + __popc(gw & below), eq_before = eqb + __popc(ew & below);
+      if (((gw >> lb) & 1u) || eq_before < need_eq) emit_pos(static_cast<int>(gt_before + min(eq_before, need_eq)), t, 32 * w + lb);
     }
   }
   if (!want_scores) return;
