@@ -188,17 +188,26 @@ struct Ring {
   }
 };
 
-// Prep threads, one row ahead: the query widened from e2m1 to e4m3 into the
-// swizzled B tile, its scale factors staged for tcgen05.cp, and for every
-// candidate block its physical page, its slot in the page and how many of its
-// positions lie below L.  The row's global reads (query, scale words, the
-// first 2048 candidate block ids) are all issued before the first wait, so
-// that their latencies overlap; the page lookups follow as one more batch.
+// Prep of a row (by the four top-k warps, two rows ahead, in that row's
+// buffers): the query widened from e2m1 to e4m3 into the swizzled B tile, its
+// scale factors staged for tcgen05.cp, and for every candidate block its
+// physical page, its slot in the page and how many of its positions lie below
+// L.  Three steps, so that the global reads overlap the top-k of the row that
+// last used the buffers: prep_issue puts the row's reads in flight (query,
+// scale words, the first 2048 candidate block ids); prep_query stages the
+// query once the MMAs of that row are done and looks up the candidates'
+// pages; prep_table writes the candidate table once that row's top-k output
+// (which reads the table) is done.
+constexpr int kPrepBatch = 16;  // candidate blocks per prep thread per batch
+struct PrepRegs {
+  uint2 qv[4];  // the query's 4 KB: 32 bytes per thread
+  uint32_t sf0, sf1;
+  int blk[kPrepBatch], pid[kPrepBatch];
+};
+static_assert(kHeads * 64 == kPrepThreads * 32, "four query words per prep thread");
+
 template <int KV, bool kMulti>
-__device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
-                                         volatile int* abort_flag) {
-  const int b = ri & 1;
-  const uint32_t ph = (ri >> 1) & 1;
+__device__ __forceinline__ void prep_issue(const SelectArgs& a, const RowInfo& r, int pid_t, PrepRegs& pr) {
   const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
   const uint8_t* q_fp4 = ly.q_fp4 + static_cast<int64_t>(r.row) * kHeads * 64;
   const uint8_t* q_sf = ly.q_sf + static_cast<int64_t>(r.row) * kHeads * 4;
@@ -206,40 +215,49 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
   pin<kMulti>(q_fp4);
   pin<kMulti>(q_sf);
   pin<kMulti>(brow);
-  // the query's 4 KB: 32 bytes per thread, as four 8-byte words
-  static_assert(kHeads * 64 == kPrepThreads * 32, "four query words per prep thread");
-  uint2 qv[4];
   if (KV == kKvMxfp4) {
     // thread slots idx = pid_t + 128 j, j < 2: head idx >> 2, 16-byte chunk idx & 3
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int idx = pid_t + kPrepThreads * j;
       const uint2* src = reinterpret_cast<const uint2*>(q_fp4 + (idx >> 2) * 64 + (idx & 3) * 16);
-      qv[2 * j] = src[0];
-      qv[2 * j + 1] = src[1];
+      pr.qv[2 * j] = src[0];
+      pr.qv[2 * j + 1] = src[1];
     }
   } else {
     // thread slots idx = pid_t + 128 j, j < 4: head idx >> 3, 8-byte chunk idx & 7
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int idx = pid_t + kPrepThreads * j;
-      qv[j] = *reinterpret_cast<const uint2*>(q_fp4 + (idx >> 3) * 64 + (idx & 7) * 8);
+      pr.qv[j] = *reinterpret_cast<const uint2*>(q_fp4 + (idx >> 3) * 64 + (idx & 7) * 8);
     }
   }
-  uint32_t sf0 = 0, sf1 = 0;
+  pr.sf0 = pr.sf1 = 0;
   if (pid_t < 32) {
     const uint32_t* sfp = reinterpret_cast<const uint32_t*>(q_sf);
-    sf0 = sfp[pid_t];
-    sf1 = sfp[32 + pid_t];
+    pr.sf0 = sfp[pid_t];
+    pr.sf1 = sfp[32 + pid_t];
   }
-  constexpr int kBatch = 16;
-  int blk[kBatch];
 #pragma unroll
-  for (int j = 0; j < kBatch; ++j) {
+  for (int j = 0; j < kPrepBatch; ++j) {
     const int i = j * kPrepThreads + pid_t;
-    blk[j] = i < r.nv ? brow[i] : -1;
+    pr.blk[j] = i < r.nv ? brow[i] : -1;
   }
-  bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
+}
+
+// Page of candidate block blk (covering positions blk << shift ..
+// + (1 << shift) - 1: 8 positions, or a context shard's 4, 2 or 1, inside one
+// 8-position group), or -1 when it has none.
+__device__ __forceinline__ int prep_page(const int32_t* pt, const RowInfo& r, int blk, int sh) {
+  return (blk >= 0 && blk < r.nb) ? pt[(blk << sh) >> 6] : -1;
+}
+
+template <int KV, bool kMulti>
+__device__ __forceinline__ bool prep_query(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
+                                           volatile int* abort_flag, PrepRegs& pr) {
+  const int b = ri & 1;
+  const uint32_t ph = (ri >> 1) & 1;
+  const bool ok = warp_wait(&sm.q_empty[b], ph ^ 1, abort_flag);  // MMAs of row ri - 2 done
   if (ok) {
     if (KV == kKvMxfp4) {
       // packed e2m1 rows of 64 bytes, 64-byte swizzle
@@ -247,53 +265,64 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
       for (int j = 0; j < 2; ++j) {
         const int idx = pid_t + kPrepThreads * j;
         *reinterpret_cast<uint4*>(sm.q[b] + sw64_offset(idx >> 2, (idx & 3) * 16)) =
-            make_uint4(qv[2 * j].x, qv[2 * j].y, qv[2 * j + 1].x, qv[2 * j + 1].y);
+            make_uint4(pr.qv[2 * j].x, pr.qv[2 * j].y, pr.qv[2 * j + 1].x, pr.qv[2 * j + 1].y);
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int idx = pid_t + kPrepThreads * j;
-        *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(idx >> 3, (idx & 7) * 16)) = widen_fp4x16(qv[j]);
+        *reinterpret_cast<uint4*>(sm.q[b] + sw128_offset(idx >> 3, (idx & 7) * 16)) = widen_fp4x16(pr.qv[j]);
       }
     }
     // lane l of the scale-factor columns: heads l and 32 + l, byte j = K block j
-    if (pid_t < 32) *reinterpret_cast<uint4*>(sm.sf[b] + 16 * pid_t) = make_uint4(sf0, sf1, kUnitScales, kUnitScales);
+    if (pid_t < 32)
+      *reinterpret_cast<uint4*>(sm.sf[b] + 16 * pid_t) = make_uint4(pr.sf0, pr.sf1, kUnitScales, kUnitScales);
   }
   fence_proxy_async_smem();
   mbar_arrive(&sm.q_full[b]);
+  const int32_t* pt = a.p.page_table + static_cast<int64_t>(row_request(a, r.row)) * a.p.max_pages;
+#pragma unroll
+  for (int j = 0; j < kPrepBatch; ++j) pr.pid[j] = prep_page(pt, r, pr.blk[j], a.block_shift);
+  return ok;
+}
+
+template <int KV, bool kMulti>
+__device__ __forceinline__ bool prep_table(Smem& sm, const SelectArgs& a, const RowInfo& r, int ri, int pid_t,
+                                           volatile int* abort_flag, bool ok, PrepRegs& pr) {
+  const int b = ri & 1;
+  const uint32_t ph = (ri >> 1) & 1;
+  const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
+  const int32_t* brow = ly.blocks + static_cast<int64_t>(r.row) * ly.blocks_stride;
+  pin<kMulti>(brow);
+  const int sh = a.block_shift;
   ok = ok && warp_wait(&sm.info_empty[b], ph ^ 1, abort_flag);  // row ri - 2 gathered and scored
-  const int req = row_request(a, r.row);
-  const int32_t* pt = a.p.page_table + static_cast<int64_t>(req) * a.p.max_pages;
-  for (int i0 = 0; ok && i0 < r.nv; i0 += kPrepThreads * kBatch) {
-    if (i0 > 0) {
+  for (int i0 = 0; ok && i0 < r.nv; i0 += kPrepThreads * kPrepBatch) {
+    if (i0 > 0) {  // rows of more than 2048 candidates: the rest in further batches
+      const int32_t* pt = a.p.page_table + static_cast<int64_t>(row_request(a, r.row)) * a.p.max_pages;
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
+      for (int j = 0; j < kPrepBatch; ++j) {
         const int i = i0 + j * kPrepThreads + pid_t;
-        blk[j] = i < r.nv ? brow[i] : -1;
+        pr.blk[j] = i < r.nv ? brow[i] : -1;
       }
+#pragma unroll
+      for (int j = 0; j < kPrepBatch; ++j) pr.pid[j] = prep_page(pt, r, pr.blk[j], sh);
     }
-    int pid[kBatch];
-    // candidate block blk covers positions blk << shift .. + (1 << shift) - 1
-    // (8 positions, or a context shard's 4, 2 or 1), inside one 8-position group
-    const int sh = a.block_shift;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) pid[j] = (blk[j] >= 0 && blk[j] < r.nb) ? pt[(blk[j] << sh) >> 6] : -1;
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
+    for (int j = 0; j < kPrepBatch; ++j) {
       const int i = i0 + j * kPrepThreads + pid_t;
       if (i >= r.nv) continue;
+      const int blk = pr.blk[j], pid = pr.pid[j];
       int v = -1;
-      if (blk[j] < 0 || (blk[j] >= r.nb && sh == 3))
+      if (blk < 0 || (blk >= r.nb && sh == 3))
         report(a.p.dev_err, kDevErrBlock);
-      else if (blk[j] >= r.nb)
+      else if (blk >= r.nb)
         ;  // a context shard holds no position of this (global) block: empty
-      else if (pid[j] < 0 || pid[j] >= a.p.num_pages)
+      else if (pid < 0 || pid >= a.p.num_pages)
         report(a.p.dev_err, kDevErrPage);
       else
-        v = (pid[j] << 10) | ((((blk[j] << sh) >> 3) & 7) << 7) | (((blk[j] << sh) & 7) << 4) |
-            min(1 << sh, r.L - (blk[j] << sh));
+        v = (pid << 10) | ((((blk << sh) >> 3) & 7) << 7) | (((blk << sh) & 7) << 4) | min(1 << sh, r.L - (blk << sh));
       sm.info[b][i] = v;
-      sm.bid[b][i] = blk[j];
+      sm.bid[b][i] = blk;
     }
   }
   mbar_arrive(&sm.info_full[b]);
@@ -303,9 +332,11 @@ __device__ __forceinline__ bool prep_row(Smem& sm, const SelectArgs& a, const Ro
 // Top-k of one row whose order keys sit in tensor memory: column t of the
 // buffer holds tile t, lane p the tile's position p (key 0 = no candidate).
 // Run by the 128 threads of warps 4-7, thread kt owning lane kt.
-template <class EmitPos, class EmitScore>
+// after_first() is called by every thread once the first pass over the keys
+// (their range) is done: other work of the same threads goes there.
+template <class EmitPos, class EmitScore, class AfterFirst>
 __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, int k, int kt, EmitPos emit_pos,
-                                          bool want_scores, EmitScore emit_score) {
+                                          bool want_scores, EmitScore emit_score, AfterFirst after_first) {
   TopkShared& sh = sm.topk;
   const int q = kt >> 5, l = kt & 31;
   uint32_t x[32];
@@ -335,6 +366,7 @@ __device__ __forceinline__ void tmem_topk(Smem& sm, uint32_t lane_col0, int nt, 
   named_sync(kTopkBar, kTopkThreads);
   mn = sm.kmin;
   mx = sm.kmax;
+  after_first();
   int hi = mn == mx ? 0 : 32 - __clz(mn ^ mx);  // low bits not shared by every live key
   uint32_t mask = hi == 32 ? 0u : ~((1u << hi) - 1u);
   uint32_t prefix = mn & mask;
@@ -772,16 +804,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ top-k of finished rows + next-row prep
     const int kt = tid - kTopkWarp0 * 32;
     const uint32_t lane_base = tmem_addr(tbase, 32 * (warp & 3), 0);
-    // prep of row index pi (the pi-th row of this CTA); the verdict is made uniform
-    // across the four warps before anyone acts on it
-    auto prep = [&](int pi) -> bool {
-      const int pu = unit_of<kMulti>(pi);
-      const bool mine = pu >= rows || prep_row<KV, kMulti>(sm, a, row_info<kMulti>(a, pu, false), pi, kt, abort_flag);
+    // the prep verdict (mine: this thread's steps succeeded) made uniform across
+    // the four warps before anyone acts on it
+    auto all_ok = [&](bool mine) -> bool {
       if (lane == 0) sm.prep_ok[warp & 3] = mine ? 1 : 0;
       named_sync(kTopkBar, kTopkThreads);
       const bool all = sm.prep_ok[0] && sm.prep_ok[1] && sm.prep_ok[2] && sm.prep_ok[3];
       named_sync(kTopkBar, kTopkThreads);
       return all;
+    };
+    // the prep of row index pi (the pi-th row of this CTA), all steps at once
+    auto prep = [&](int pi) -> bool {
+      const int pu = unit_of<kMulti>(pi);
+      bool mine = true;
+      if (pu < rows) {
+        const RowInfo rp = row_info<kMulti>(a, pu, false);
+        PrepRegs pr;
+        prep_issue<KV, kMulti>(a, rp, kt, pr);
+        mine = prep_query<KV, kMulti>(sm, a, rp, pi, kt, abort_flag, pr);
+        mine = prep_table<KV, kMulti>(sm, a, rp, pi, kt, abort_flag, mine, pr);
+      }
+      return all_ok(mine);
     };
     bool ok = prep(0) && prep(1);
     int ri = 0;
@@ -789,6 +832,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const RowInfo r = row_info<kMulti>(a, u, false);
       const SelectLayer& ly = layer_of<kMulti>(a, r.layer);
       const int b = ri & 1;
+      // row ri + 2 is prepared in this row's buffers around its top-k: reads
+      // issued now, the query staged after the top-k's first pass, the table
+      // written after the top-k's output
+      const int u2 = unit_of<kMulti>(ri + 2);
+      const bool has2 = u2 < rows;
+      RowInfo r2 = {};
+      PrepRegs pr;
+      if (has2) {
+        r2 = row_info<kMulti>(a, u2, false);
+        prep_issue<KV, kMulti>(a, r2, kt, pr);
+      }
+      bool mine = true;
+      auto stage_query = [&]() {
+        if (has2) mine = prep_query<KV, kMulti>(sm, a, r2, ri + 2, kt, abort_flag, pr);
+      };
       if (kt == 0) sm.topk_go = mbar_wait(&sm.sc_full[b], (ri >> 1) & 1, abort_flag) ? 1 : 0;
       named_sync(kTopkBar, kTopkThreads);
       if (!sm.topk_go) {
@@ -808,7 +866,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int i = t * kBlocksPerTile + (p >> 3);
               out[rank] = (sm.bid[b][i] << a.block_shift) + (p & 7) - ((sm.info[b][i] >> 4) & 7);
             },
-            osc != nullptr, [&](int rank, uint32_t u) { osc[rank] = order_key_inv(u); });
+            osc != nullptr, [&](int rank, uint32_t u) { osc[rank] = order_key_inv(u); }, stage_query);
+      } else {
+        stage_query();
       }
       for (int i = max(k, 0) + kt; i < a.topk; i += kTopkThreads) {
         out[i] = -1;
@@ -820,7 +880,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.vcount[b] = 0;
         mbar_arrive(&sm.sc_empty[b]);
       }
-      ok = prep(ri + 2);
+      if (has2) mine = prep_table<KV, kMulti>(sm, a, r2, ri + 2, kt, abort_flag, mine, pr);
+      ok = all_ok(mine);
     }
     if (!ok && kt == 0) set_abort(sm, a.p.dev_err);
   } else if (warp >= kScoreWarp0) {
