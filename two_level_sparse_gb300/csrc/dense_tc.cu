@@ -132,6 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MXFP4 scales are read by the MMA warp, in order, before it issues tile u,
   // so they never need a release either.
   constexpr bool kScaleRelease = R != 3 && !kFp4;
+  // FP8 K, three rows: a tile's scale copies complete on the K tile's own
+  // barrier.  The epilogue reads them once the tile's accumulator is full,
+  // which follows the MMA warp's wait on that barrier, so it waits on no
+  // scale barrier of its own.
+  constexpr bool kScaleOnK = !kFp4 && !kScaleRelease;
   constexpr bool kAbsAdd = scorer_relu_abs_add<KV>();  // ReLU form: identical to the sparse scorer's
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -370,14 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t nvalid = (pid[0] >= 0) + (pid[1] >= 0);
-          mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * kPVB);
-          mbar_arrive_expect_tx_elect(&sm.s_full[si], nvalid * kPage * 4);
+          uint64_t* const sbar = kScaleOnK ? &sm.k_full[ki] : &sm.s_full[si];
+          if (kScaleOnK) {
+            mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * (kPVB + kPage * 4));
+          } else {
+            mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * kPVB);
+            mbar_arrive_expect_tx_elect(&sm.s_full[si], nvalid * kPage * 4);
+          }
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (pid[j] < 0) continue;
             tma_load_3d_elect(sm.kv[ki] + j * kPVB, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
             bulk_load_elect(&sm.ks[si][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPB + kPVB, kPage * 4,
-                            &sm.s_full[si]);
+                            sbar);
           }
           issued = ts + 1;
         }
@@ -472,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float score = head_reduce_finish<kAbsAdd>(part);
         float kscale = 1.0f;  // MXFP4: the scales are inside the MMA
         if (!kFp4) {
-          if (!warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
+          if (!kScaleOnK && !warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
             if (lane == 0) set_abort(sm, a.p.dev_err);
             return false;
           }
@@ -550,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
         if ((i & 1u) != par) continue;
         mbar_wait(&sm.k_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
-        mbar_wait(&sm.s_full[i % kScaleSlots], (i / kScaleSlots) & 1, nullptr, 1000000000ull);
+        if (!kScaleOnK) mbar_wait(&sm.s_full[i % kScaleSlots], (i / kScaleSlots) & 1, nullptr, 1000000000ull);
       }
     }
   }
