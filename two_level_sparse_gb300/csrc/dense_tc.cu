@@ -16,7 +16,8 @@
 //               64-position pages of FP8 K per
 //               128-position tile (one tensor-map load each, 128-byte
 //               swizzle) into an 8-stage ring, their fp32 scales (bulk
-//               copies) into a separate 16-slot ring;
+//               copies) into a separate 16-slot ring, both completing on
+//               the K stage's barrier;
 //   warp 1      MMA issuer: tcgen05.mma kind::mxf8f6f4 block_scale, M = 128
 //               positions, N = 64 R columns (R rows x 64 heads), K = 128 in
 //               four K = 32 steps; A = K tile (scale 1), B = the rows' queries
@@ -62,7 +63,7 @@ struct __align__(1024) Smem {
   uint8_t q[3 * kHeads * kDim];        // B tile (up to 192 rows of 128 B)
   float ks[kScaleSlots][kTileM];       // per-position K scales
   uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t s_full[kScaleSlots], s_empty[kScaleSlots];
+  uint64_t s_empty[kScaleSlots];  // scale slot read by every epilogue warp (one-row groups only)
   uint64_t t_full[4], t_empty[4];
   uint64_t drain;
   uint32_t tmem_base;
@@ -132,11 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MXFP4 scales are read by the MMA warp, in order, before it issues tile u,
   // so they never need a release either.
   constexpr bool kScaleRelease = R != 3 && !kFp4;
-  // FP8 K, three rows: a tile's scale copies complete on the K tile's own
-  // barrier.  The epilogue reads them once the tile's accumulator is full,
-  // which follows the MMA warp's wait on that barrier, so it waits on no
-  // scale barrier of its own.
-  constexpr bool kScaleOnK = !kFp4 && !kScaleRelease;
   constexpr bool kAbsAdd = scorer_relu_abs_add<KV>();  // ReLU form: identical to the sparse scorer's
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,7 +150,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.k_empty[s], 1);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
-      mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.s_empty[s], 4 * kEpiPerTile);
     }
     for (int s = 0; s < kNumAcc; ++s) {
@@ -375,19 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t nvalid = (pid[0] >= 0) + (pid[1] >= 0);
-          uint64_t* const sbar = kScaleOnK ? &sm.k_full[ki] : &sm.s_full[si];
-          if (kScaleOnK) {
-            mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * (kPVB + kPage * 4));
-          } else {
-            mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * kPVB);
-            mbar_arrive_expect_tx_elect(&sm.s_full[si], nvalid * kPage * 4);
-          }
+          // the tile's scale words complete on its K barrier: the MMA warp
+          // waits on it before the MMAs (MXFP4 stages the words from there),
+          // and the epilogue reads the scales once the accumulator is full,
+          // which follows that wait
+          mbar_arrive_expect_tx_elect(&sm.k_full[ki], nvalid * (kPVB + kPage * 4));
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (pid[j] < 0) continue;
             tma_load_3d_elect(sm.kv[ki] + j * kPVB, &tmap, 0, 0, pid[j], &sm.k_full[ki]);
             bulk_load_elect(&sm.ks[si][j * kPage], a.p.k_pool + static_cast<int64_t>(pid[j]) * kPB + kPVB, kPage * 4,
-                            sbar);
+                            &sm.k_full[ki]);
           }
           issued = ts + 1;
         }
@@ -408,9 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = off; t < off + take; ++t, ++ts) {
         const uint32_t ki = ts & (kStages - 1), kp = (ts / kStages) & 1;
         const uint32_t ai = ts & (kNumAcc - 1), ap = (ts / kNumAcc) & 1;
-        const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+        const uint32_t si = ts & (kScaleSlots - 1);
         if (!warp_wait_fast(&sm.k_full[ki], kp, abort_flag) ||
-            (kFp4 && !warp_wait_fast(&sm.s_full[si], sp, abort_flag)) ||
             !warp_wait_fast(&sm.t_empty[ai], ap ^ 1, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           break;
@@ -461,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto tile = [&](int t, uint32_t ts, uint32_t ai, auto interior) -> bool {
         constexpr bool kIn = decltype(interior)::value;
         const uint32_t ap = (ts / kNumAcc) & 1;
-        const uint32_t si = ts & (kScaleSlots - 1), sp = (ts / kScaleSlots) & 1;
+        const uint32_t si = ts & (kScaleSlots - 1);
         if (!warp_wait_fast(&sm.t_full[ai], ap, abort_flag)) {
           if (lane == 0) set_abort(sm, a.p.dev_err);
           return false;
@@ -482,10 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float score = head_reduce_finish<kAbsAdd>(part);
         float kscale = 1.0f;  // MXFP4: the scales are inside the MMA
         if (!kFp4) {
-          if (!kScaleOnK && !warp_wait_fast(&sm.s_full[si], sp, abort_flag)) {
-            if (lane == 0) set_abort(sm, a.p.dev_err);
-            return false;
-          }
           kscale = lds_f32(ks0 + si * (kTileM * 4));
         }
         if (kScaleRelease) {
@@ -560,7 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
         if ((i & 1u) != par) continue;
         mbar_wait(&sm.k_full[i % kStages], (i / kStages) & 1, nullptr, 1000000000ull);
-        if (!kScaleOnK) mbar_wait(&sm.s_full[i % kScaleSlots], (i / kScaleSlots) & 1, nullptr, 1000000000ull);
       }
     }
   }
