@@ -30,11 +30,13 @@
 //               the same warp stages the 128 positions' scale words for the
 //               MMA warp's tcgen05.cp with 4-byte cp.async;
 //   warps 4-7   top-k of the previous row, read back from tensor memory, and
-//               then, two rows ahead, the page of every candidate block, the
-//               query (widened from e2m1 to e4m3 against FP8 K, packed against
-//               MXFP4 K) and its scale factors staged;
+//               around it the prep of the row two ahead in the buffers it
+//               frees: the page of every candidate block, the query (widened
+//               from e2m1 to e4m3 against FP8 K, packed against MXFP4 K) and
+//               its scale factors staged;
 //   warps 8-15  two scoring warpgroups, tiles alternating: each thread loads
-//               its position's FP8 K scale straight from the pool, then the
+//               its position's FP8 K scale from the pool (straight when the
+//               pool fits in L2, a few tiles ahead through a ring otherwise), then the
 //               same epilogue arithmetic as the dense pass and one
 //               order-preserving key per candidate stored as one
 //               tensor-memory column per tile.
