@@ -767,7 +767,7 @@ def rooflines(a, b):
 RECORDED_TRAFFIC = {
     # mean of the five launches of a step: 225.2 MB read (the pool once, queries, ids) + 26.9 MB written
     "select_kernel": {"bytes_per_launch": 252.1e6, "sources": ("sparse_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
-                      "sha256": "ca34f6bcbff85e1bf1b04c58c38d7cd161545e364e8352290c9ba80e07cbbd18"},
+                      "sha256": "260b09aec96763ecf42d977280a92a910bd2309dad15b89c665636806668752d"},
     # 132.0 MB read (pool, queries) + 2043.2 MB written (keys)
     "dense_amax8_kernel": {"bytes_per_launch": 2175.2e6, "sources": ("dense_tc.cu", "ci_common.cuh", "sm103_ptx.cuh"),
                            "sha256": "04ede5c13a743f10245fdc058c787aa95c36d0e42882d69cb6934585553fbab3"},
