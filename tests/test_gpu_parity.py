@@ -74,6 +74,48 @@ def test_small_prefill_all_rows(ci, rows, base, K):
 
 
 @needs_cuda
+@pytest.mark.parametrize("layout,lens", [
+    (synth.LAYOUT_DECODE, [3000, 5001, 9000, 700]),
+    (synth.LAYOUT_PREFILL, [6000 + 37 * i for i in range(5)]),
+])
+def test_position_ties_go_to_the_lower_position(ci, layout, lens):
+    """Pools of four distinct K vectors with one scale: a row's scores take
+    four values, so every top-512 cuts through a long run of bit-identical
+    scores.  The source layer's positions must equal the dense definition's
+    and each consumer's the oracle's top-512 of its candidates exactly:
+    score descending, ties toward the lower position (sglang PR #40352,
+    Design, "Level two"; the source keeps P + 1 blocks, so its top-P is the
+    dense one even through ties)."""
+    wl = synth.make_workload("ties", layout, lens, topk_blocks=128, seed=71, topk=512)
+    rng = np.random.default_rng(72)
+    for ly in wl.layers:
+        pages = ly.k_pool.numpy().reshape(-1, O.PAGE_BYTES)  # shares the tensor's memory
+        vals = pages[:, : O.PAGE_VALUE_BYTES].reshape(-1, O.PAGE, O.D)
+        scales = pages[:, O.PAGE_VALUE_BYTES :].view("<f4")
+        four = vals[0, :4].copy()
+        vals[:] = four[rng.integers(0, 4, size=vals.shape[:2])]
+        scales[:] = np.float32(0.75)
+    step = run_step(wl)
+    assert int(step.dev_err.item()) == 0
+    out = step.outputs_numpy()
+    pt, row_req, P = wl.page_table.numpy(), wl.row_req(), wl.topk
+    cut_ties = 0
+    for t, L in enumerate(wl.seq_len.tolist()):
+        logit, _ = O.dense_row_scores(wl.layers[0], pt, wl.layout, t, L, row_req)
+        want = O.top_positions(logit, np.arange(L), P)
+        np.testing.assert_array_equal(out["pos"][0][t], want, err_msg=f"row {t} layer 0")
+        if L > P:
+            kth = logit[want[want >= 0]].min()
+            cut_ties += int(np.sum(logit == kth) > np.sum(logit[want[want >= 0]] == kth))
+        blocks, nv = np.asarray(out["blocks"][t], dtype=np.int64), int(out["nvalid"][t])
+        for j in range(1, len(wl.layers)):
+            want_j, _, _, _ = O.select_row(wl.layers[j], pt, wl.layout, t, L, blocks, nv, P, row_req)
+            np.testing.assert_array_equal(out["pos"][j][t], want_j, err_msg=f"row {t} layer {j}")
+    assert cut_ties > 0  # the threshold did fall inside a run of ties
+    assert_ok(compare.check_step(wl, out))
+
+
+@needs_cuda
 def test_duplicate_blocks_score_bit_identically(ci):
     # every copy of a block must get bit-identical keys (the tie rule needs it)
     wl = synth.make_workload("dup", synth.LAYOUT_DECODE, [4000, 3000], topk_blocks=16, seed=9, dup_frac=0.2)
