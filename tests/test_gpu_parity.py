@@ -18,6 +18,7 @@ from two_level_sparse_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")
+MX = synth.KV_MXFP4
 
 
 @pytest.fixture(scope="module")
@@ -73,28 +74,46 @@ def test_small_prefill_all_rows(ci, rows, base, K):
     assert_ok(compare.check_step(wl, step.outputs_numpy()))
 
 
-@needs_cuda
-@pytest.mark.parametrize("layout,lens", [
-    (synth.LAYOUT_DECODE, [3000, 5001, 9000, 700]),
-    (synth.LAYOUT_PREFILL, [6000 + 37 * i for i in range(5)]),
-])
-def test_position_ties_go_to_the_lower_position(ci, layout, lens):
-    """Pools of four distinct K vectors with one scale: a row's scores take
-    four values, so every top-512 cuts through a long run of bit-identical
-    scores.  The source layer's positions must equal the dense definition's
-    and each consumer's the oracle's top-512 of its candidates exactly:
-    score descending, ties toward the lower position (sglang PR #40352,
-    Design, "Level two"; the source keeps P + 1 blocks, so its top-P is the
-    dense one even through ties)."""
-    wl = synth.make_workload("ties", layout, lens, topk_blocks=128, seed=71, topk=512)
-    rng = np.random.default_rng(72)
+def _four_vector_pools(wl, seed):
+    """Every layer's pool rewritten so that each position holds one of four K
+    vectors (values and scale bytes together; FP8 pools get one fp32 scale)."""
+    rng = np.random.default_rng(seed)
     for ly in wl.layers:
-        pages = ly.k_pool.numpy().reshape(-1, O.PAGE_BYTES)  # shares the tensor's memory
-        vals = pages[:, : O.PAGE_VALUE_BYTES].reshape(-1, O.PAGE, O.D)
-        scales = pages[:, O.PAGE_VALUE_BYTES :].view("<f4")
-        four = vals[0, :4].copy()
-        vals[:] = four[rng.integers(0, 4, size=vals.shape[:2])]
-        scales[:] = np.float32(0.75)
+        if O.is_mxfp4_pool(ly.k_pool.numpy()):
+            pages = ly.k_pool.numpy().reshape(-1, O.PAGE_BYTES_MXFP4)  # shares the tensor's memory
+            vals = pages[:, : O.PAGE_VALUE_BYTES_MXFP4].reshape(-1, O.PAGE, O.D // 2)
+            scales = pages[:, O.PAGE_VALUE_BYTES_MXFP4 :].reshape(-1, O.PAGE, O.D // 32)
+            pick = rng.integers(0, 4, size=vals.shape[:2])
+            four_v, four_s = vals[0, :4].copy(), scales[0, :4].copy()
+            vals[:] = four_v[pick]
+            scales[:] = four_s[pick]
+        else:
+            pages = ly.k_pool.numpy().reshape(-1, O.PAGE_BYTES)
+            vals = pages[:, : O.PAGE_VALUE_BYTES].reshape(-1, O.PAGE, O.D)
+            four = vals[0, :4].copy()
+            vals[:] = four[rng.integers(0, 4, size=vals.shape[:2])]
+            pages[:, O.PAGE_VALUE_BYTES :].view("<f4")[:] = np.float32(0.75)
+
+
+@needs_cuda
+@pytest.mark.parametrize("case", ["decode", "prefill", "varlen", "decode_mxfp4", "prefill_mxfp4"])
+def test_position_ties_go_to_the_lower_position(ci, case):
+    """Pools of four distinct K vectors: a row's scores take four values, so
+    every top-512 cuts through a long run of bit-identical scores.  The
+    source layer's positions must equal the dense definition's and each
+    consumer's the oracle's top-512 of its candidates exactly: score
+    descending, ties toward the lower position (sglang PR #40352, Design,
+    "Level two"; the source keeps P + 1 blocks, so its top-P is the dense one
+    even through ties)."""
+    kv = MX if case.endswith("mxfp4") else synth.KV_FP8
+    if case.startswith("decode"):
+        wl = synth.make_workload("ties", synth.LAYOUT_DECODE, [3000, 5001, 9000, 700], 128, seed=71, kv=kv)
+    elif case.startswith("prefill"):
+        wl = synth.make_workload("ties", synth.LAYOUT_PREFILL, [6000 + 37 * i for i in range(5)], 128, seed=73,
+                                 kv=kv)
+    else:
+        wl = synth.make_varlen_workload("ties", (2000, 0, 7000), (2, 3, 2), 128, seed=75)
+    _four_vector_pools(wl, 72)
     step = run_step(wl)
     assert int(step.dev_err.item()) == 0
     out = step.outputs_numpy()
@@ -513,7 +532,6 @@ def test_prefill_tail_after_a_varlen_step_matches_the_oracle(ci):
 
 
 # ----------------------------------------------------------------------------- MXFP4 index-K
-MX = synth.KV_MXFP4
 
 
 @needs_cuda
