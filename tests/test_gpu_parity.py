@@ -96,7 +96,8 @@ def _four_vector_pools(wl, seed):
 
 
 @needs_cuda
-@pytest.mark.parametrize("case", ["decode", "prefill", "varlen", "decode_mxfp4", "prefill_mxfp4"])
+@pytest.mark.parametrize("case", ["decode", "prefill", "varlen", "decode_mxfp4", "prefill_mxfp4", "decode_dcp2",
+                                  "prefill_dcp4"])
 def test_position_ties_go_to_the_lower_position(ci, case):
     """Pools of four distinct K vectors: a row's scores take four values, so
     every top-512 cuts through a long run of bit-identical scores.  The
@@ -104,7 +105,9 @@ def test_position_ties_go_to_the_lower_position(ci, case):
     consumer's the oracle's top-512 of its candidates exactly: score
     descending, ties toward the lower position (sglang PR #40352, Design,
     "Level two"; the source keeps P + 1 blocks, so its top-P is the dense one
-    even through ties)."""
+    even through ties).  The context-sharded cases take the same positions
+    through the exact merge across shards (vLLM sparse_attn_indexer.py,
+    _merge_dcp_topk_global: a stable top-k over (score, global id))."""
     kv = MX if case.endswith("mxfp4") else synth.KV_FP8
     if case.startswith("decode"):
         wl = synth.make_workload("ties", synth.LAYOUT_DECODE, [3000, 5001, 9000, 700], 128, seed=71, kv=kv)
@@ -114,7 +117,14 @@ def test_position_ties_go_to_the_lower_position(ci, case):
     else:
         wl = synth.make_varlen_workload("ties", (2000, 0, 7000), (2, 3, 2), 128, seed=75)
     _four_vector_pools(wl, 72)
-    step = run_step(wl)
+    if "dcp" in case:
+        from two_level_sparse_gb300.dcp import DcpStep
+
+        step = DcpStep(wl.to("cuda"), int(case[-1]))
+        step.run()
+        torch.cuda.synchronize()
+    else:
+        step = run_step(wl)
     assert int(step.dev_err.item()) == 0
     out = step.outputs_numpy()
     pt, row_req, P = wl.page_table.numpy(), wl.row_req(), wl.topk
