@@ -499,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
           if (kIn) {
-            if ((lane & 7) == 0) kp_row[t * (kTileM / kBlock)] = v;
+            // every lane of a block's 8 holds its maximum: all store (one
+            // 16-byte segment per warp), no predicate
+            kp_row[t * (kTileM / kBlock)] = v;
           } else if ((lane & 7) == 0 && pos < rlen) {
             kp_row[t * (kTileM / kBlock)] = (pos >> 3) == nb - 1 ? __int_as_float(0x7f800000) : v;
           }
