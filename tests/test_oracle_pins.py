@@ -327,6 +327,29 @@ def test_top_positions_bruteforce_ranks():
         assert np.all(out[len(expect):] == -1)
 
 
+def test_source_top_p_through_p_plus_1_blocks_equals_dense_top_p():
+    """The source layer keeps its own top-(P + 1) blocks (newest pinned) and
+    takes its top-P positions inside them; that equals the top-P over every
+    position, ties toward the lower position included, because every block
+    holding a position above the P-th score outranks the rest and the blocks
+    of the tied positions taken come first in id order (sglang PR #40352,
+    Design: the source's own top-512 through K' = P + 1 candidate blocks).
+    Checked by brute force on rows of heavily tied integer scores."""
+    rng = np.random.default_rng(7)
+    for trial in range(800):
+        L = int(rng.integers(1, 160))
+        P = int(rng.integers(1, 14))
+        sc = rng.integers(0, 3, L).astype(np.float64)
+        nb = O.num_blocks(L)
+        keys, _ = O.block_keys(sc, L)
+        blocks, nvalid = O.select_blocks(keys, nb, P + 1)
+        cand = O.candidate_positions(blocks, nvalid, L)
+        two_level = O.top_positions(sc[cand], cand, P)
+        dense = sorted(int(i) for i in range(L) if _rank(sc, i) < P)
+        assert two_level[: len(dense)].tolist() == dense
+        assert np.all(two_level[len(dense):] == -1)
+
+
 def test_two_level_fixture():
     (L,), src, blocks_expect, cons, pos_expect = _read_fixture("two_level_example.txt")
     L = int(L)
