@@ -35,7 +35,7 @@
 // scale in the epilogue.
 // Prefill rows share one request's pages, so R = 3 rows ride one MMA
 // (N = 192, two accumulator stages); decode rows each have their own pages,
-// R = 1 (N = 64, six stages) and the three epilogue warpgroups take tiles
+// R = 1 (N = 64, four stages) and the three epilogue warpgroups take tiles
 // round-robin.  Work is the list of (row group, 128-position tile) pairs,
 // split evenly across the CTAs.
 #include <type_traits>
